@@ -1,0 +1,199 @@
+/*
+ * fgf8.h -- C ABI of the fine-grained FP8 library for B300 (sm_103a).
+ *
+ * Fine-grained FP8 quantization and block-scaled FP8 GEMM, after the
+ * DeepSeek-V3 FP8 training scheme as described on the pages cited below:
+ *   [dssusan]  "dssusan.co.kr Q&A post 93378" -- Figure 7(a) passage (1x128
+ *              activation tiles, 128x128 weight blocks), inner-dimension
+ *              passage (per-group scales along K; about 14 accumulated bits
+ *              on H800), Figure 7(b) passage (FP8 inputs, BF16 or FP32
+ *              outputs, promotion of partial sums to FP32), E4M3 passage
+ *              (E4M3 on all tensors, FP8 Wgrad, dequantization by scale
+ *              multiplication on CUDA cores).
+ *   [kailasan] "kailasan.com recruit post 147436" -- hardware-suggestion
+ *              passage (at each promotion interval the partial results are
+ *              multiplied by the scaling factors and added to FP32).
+ *   [why-be]   "why-be.co.kr A/S post 36949" -- FP8-cast-with-TMA and
+ *              transposed-read passages (quantization round trip through HBM;
+ *              transposed copies for the backward pass).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  Outputs are valid once the stream reaches
+ *     that point.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns an error code and launches nothing.  A launch
+ *     failure returns FGF8_ERR_CUDA.
+ *   - Matrices are row-major with the stated leading dimension (in
+ *     elements).  E4M3 tensors are one byte per element (OCP E4M3 codes).
+ *   - Scale tensors are "K-group major": the scales of one K group (or token
+ *     group) are contiguous, so that one aligned copy serves a whole tile.
+ *     Every scale leading dimension must be a multiple of 4 (16 bytes).
+ *   - Outputs must not alias inputs.  Inputs are assumed finite.
+ *   - The library runs only on compute capability 10.3 (B300, sm_103a);
+ *     other devices get FGF8_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef FGF8_H
+#define FGF8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FGF8_OK = 0,
+    FGF8_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum, bad stride */
+    FGF8_ERR_MISALIGNED = 2,         /* a pointer or row stride breaks the 16-byte rule */
+    FGF8_ERR_UNSUPPORTED_SHAPE = 3,  /* e.g. K % 128 != 0, N % 16 != 0 */
+    FGF8_ERR_UNSUPPORTED_DEVICE = 4, /* not a compute capability 10.3 device */
+    FGF8_ERR_WORKSPACE_TOO_SMALL = 5,
+    FGF8_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed */
+    FGF8_ERR_TIMEOUT = 7             /* a device-side wait gave up (see fgf8_read_status) */
+} fgf8_status;
+
+typedef enum { FGF8_OUT_BF16 = 0, FGF8_OUT_FP32 = 1 } fgf8_out_dtype;
+
+typedef enum {
+    /* one scale per 128x128 block of B: sb[kb*ldsb + n/128] ([dssusan] Figure 7(a)) */
+    FGF8_BSCALE_BLOCK128 = 0,
+    /* one scale per row of B per 128-wide K group: sb[kb*ldsb + n]
+     * (B quantized in 128x1 tiles along K, as for the weight-gradient GEMM) */
+    FGF8_BSCALE_ROW1x128 = 1
+} fgf8_bscale_kind;
+
+/* Human-readable name of a status code (static string). */
+const char *fgf8_status_string(fgf8_status st);
+
+/* Library version string (static). */
+const char *fgf8_version(void);
+
+/*
+ * fp8_quant_act_1x128 -- activation quantization in 1x128 tiles (per token per
+ * 128 channels), [dssusan] Figure 7(a) passage, with the optional transposed
+ * 128x1 output kept for the weight-gradient GEMM ([dssusan] E4M3 passage, FP8
+ * Wgrad; [why-be] transposed-read passage).
+ *
+ * For each group g of 128 values: amax = max|x|; s = amax / 448 (binary32
+ * division); q = E4M3(fl32(x / s)) with round-to-nearest-even and saturation
+ * to +-448; an all-zero group gives s = 0 and signed zeros.
+ *
+ *   x   : BF16 [M][ldx], ldx >= K.  K % 128 == 0.  M >= 0 (M == 0: no-op).
+ *   q   : E4M3 [M][K] (row stride K), groups along K;           may be NULL
+ *   s   : float [K/128][lds], s[kb*lds + m]; lds >= M, lds % 4 == 0;  NULL iff q is
+ *   qT  : E4M3 [K][M] (row stride M), groups of 128 tokens along M (the last
+ *         group may be partial: amax over the tokens present);       may be NULL
+ *   sT  : float [ceil(M/128)][ldsT], sT[tb*ldsT + k]; ldsT >= K, ldsT % 4 == 0; NULL iff qT is
+ * At least one of q, qT must be given.  x must be 8-byte aligned with ldx % 4
+ * == 0; q, s, qT, sT 16-byte aligned; with qT given, M % 16 == 0.
+ */
+fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                uint8_t *q, float *s, int64_t lds,
+                                uint8_t *qT, float *sT, int64_t ldsT,
+                                void *stream);
+
+/*
+ * fp8_quant_w_128x128 -- weight quantization in 128x128 blocks (per 128 input
+ * channels per 128 output channels), [dssusan] Figure 7(a) passage.  Same rule
+ * as above with amax over the block; a ragged last block row (N % 128 != 0)
+ * takes amax over the rows present.
+ *
+ *   w : BF16 [N][ldw], ldw >= K, ldw % 4 == 0, 8-byte aligned.  K % 128 == 0.
+ *   q : E4M3 [N][K], 16-byte aligned.
+ *   s : float [K/128][lds], s[kb*lds + nb]; lds >= ceil(N/128), lds % 4 == 0.
+ */
+fgf8_status fp8_quant_w_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                uint8_t *q, float *s, int64_t lds, void *stream);
+
+/*
+ * fp8_gemm_blockscaled -- C = A_hat * B_hat^T with per-group scales along the
+ * inner dimension K ([dssusan] inner-dimension and E4M3 passages).  Each
+ * 128-wide K partial product P = sum_{k in group} qa*qb is formed on the
+ * tensor cores, multiplied by its scale pair and added into FP32 ([kailasan]
+ * hardware-suggestion passage; [dssusan] Figure 7(b) passage):
+ *   C[m][n] = sum_kb P_kb[m][n] * sa[kb*ldsa + m] * sb_kb(n)
+ * with sb_kb(n) = sb[kb*ldsb + n/128] (BLOCK128) or sb[kb*ldsb + n] (ROW1x128).
+ *
+ *   A  : E4M3 [M][K] (row stride K), 16-byte aligned.  M >= 1.
+ *   sa : float [K/128][ldsa], ldsa >= M, ldsa % 4 == 0.
+ *   B  : E4M3 [N][K], 16-byte aligned.  N % 16 == 0.  K % 128 == 0, K >= 128.
+ *   sb : float [K/128][ldsb]; ldsb >= ceil(N/128) (BLOCK128) or >= N (ROW1x128);
+ *        ldsb % 4 == 0.
+ *   C  : [M][ldc] BF16 (cdt = FGF8_OUT_BF16) or FP32 (FGF8_OUT_FP32); ldc >= N,
+ *        ldc * element size % 16 == 0, 16-byte aligned.
+ *   workspace : device scratch of at least fgf8_gemm_workspace_bytes(M, N, K, 1)
+ *        bytes, 256-byte aligned, ZERO-FILLED before its first use.  It holds
+ *        the device status word and, for small M, the split-K partial sums
+ *        and arrival counters.  The kernels leave it ready for the next call
+ *        (counters back at zero) unless a call reports FGF8_ERR_TIMEOUT, after
+ *        which it must be zero-filled again.  One workspace must not be used
+ *        by two calls that can run at the same time.
+ */
+fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa,
+                                 const uint8_t *B, const float *sb, int64_t ldsb,
+                                 fgf8_bscale_kind bkind,
+                                 void *C, int64_t ldc, fgf8_out_dtype cdt,
+                                 int64_t M, int64_t N, int64_t K,
+                                 void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * fp8_grouped_gemm_blockscaled -- MoE expert GEMM in the contiguous layout:
+ * the rows of A are grouped by expert, each group padded to a multiple of 128
+ * rows, and row m uses expert e = m_indices[m] ([dssusan] scheme applied per
+ * expert; the MoE part loads one expert's parameters at a time, [kailasan]
+ * micro-batch passage).
+ *
+ *   A         : E4M3 [M_total][K], M_total % 128 == 0.
+ *   sa        : float [K/128][ldsa], ldsa >= M_total, ldsa % 4 == 0.
+ *   B         : E4M3 [num_experts][N][K] (expert-major, contiguous).
+ *   sb        : float [num_experts][K/128][ldsb], 128x128 block scales per
+ *               expert, ldsb >= ceil(N/128), ldsb % 4 == 0.
+ *   m_indices : int32 [M_total], expert id per row or -1 for a padding row;
+ *               all rows of one 128-row block carry the same id (or -1).
+ *               Rows of a block whose id is -1 are not written.
+ *   C         : [M_total][ldc], as for fp8_gemm_blockscaled.
+ *   workspace : at least fgf8_gemm_workspace_bytes(M_total, N, K, num_experts).
+ */
+fgf8_status fp8_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa,
+                                         const uint8_t *B, const float *sb, int64_t ldsb,
+                                         const int32_t *m_indices, int32_t num_experts,
+                                         void *C, int64_t ldc, fgf8_out_dtype cdt,
+                                         int64_t M_total, int64_t N, int64_t K,
+                                         void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace size (bytes) needed by the GEMM entry points for this shape. */
+size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
+
+/*
+ * fgf8_read_status -- synchronizes `stream`, then returns the device status
+ * word held in `workspace` (FGF8_OK, or FGF8_ERR_TIMEOUT if a bounded
+ * device-side wait expired) and resets it to FGF8_OK.  `site` (may be NULL)
+ * receives the id of the wait that expired (0 if none).
+ */
+fgf8_status fgf8_read_status(void *workspace, void *stream, int32_t *site);
+
+/*
+ * fgf8_mma_probe -- accumulation-precision probe for the tensor cores
+ * ([dssusan] inner-dimension passage: about 14 bits kept on H800; "jp-study.kr
+ * Q&A post 309256", Hopper fixed-point accumulation passage).  One CTA
+ * computes D = A * B^T with E4M3 operands and no scaling, chaining K/32
+ * tensor-core MMAs (K = 32 each) into one FP32 accumulator in tensor memory,
+ * and writes D without any promotion, so that the caller can compare it with
+ * the exact sum.
+ *
+ *   A : E4M3 [128][K]; B : E4M3 [N][K]; K % 128 == 0, 128 <= K <= 16384;
+ *   N % 16 == 0, 16 <= N <= 256.  D : float [128][N].  16-byte aligned.
+ *   workspace : >= 256 bytes, zero-filled (status word, as above).
+ */
+fgf8_status fgf8_mma_probe(const uint8_t *A, const uint8_t *B, float *D,
+                           int32_t N, int32_t K, void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGF8_H */
