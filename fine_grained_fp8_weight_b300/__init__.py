@@ -1,0 +1,202 @@
+"""Fine-grained FP8 quantization and block-scaled FP8 GEMM for B300 (sm_103a).
+
+Thin ctypes binding over ``libfgf8.so`` (the C ABI in ``include/fgf8.h``).
+The functions here only marshal arguments: they allocate outputs with torch,
+pass raw device pointers and the current CUDA stream to the library, and turn
+a non-zero status into an exception.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU or library fallback, and importing
+this package fails if the library has not been built.
+
+Scale layouts ("K-group major", as in the C header):
+  activation 1x128 scales  s  [K/128, round_up(M, 4)]
+  activation 128x1 scales  sT [ceil(M/128), round_up(K, 4)]
+  weight 128x128 scales    s  [K/128, round_up(ceil(N/128), 4)]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "FGF8Error", "lib", "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+    "fp8_grouped_gemm_blockscaled", "fgf8_mma_probe", "fgf8_read_status", "workspace_for",
+    "BSCALE_BLOCK128", "BSCALE_ROW1x128", "OUT_BF16", "OUT_FP32",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfgf8.so")
+
+BSCALE_BLOCK128 = 0
+BSCALE_ROW1x128 = 1
+OUT_BF16 = 0
+OUT_FP32 = 1
+
+STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED",
+                3: "FGF8_ERR_UNSUPPORTED_SHAPE", 4: "FGF8_ERR_UNSUPPORTED_DEVICE",
+                5: "FGF8_ERR_WORKSPACE_TOO_SMALL", 6: "FGF8_ERR_CUDA", 7: "FGF8_ERR_TIMEOUT"}
+
+# Every symbol declared in include/fgf8.h and include/fgf8_testing.h.
+EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
+            "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled", "fgf8_gemm_workspace_bytes",
+            "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout"]
+
+
+class FGF8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types declared (no compute call)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libfgf8.so is not built ({LIB_PATH}); run "
+                              "`python -m fine_grained_fp8_weight_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        L.fgf8_status_string.argtypes = [ctypes.c_int]
+        L.fgf8_status_string.restype = ctypes.c_char_p
+        L.fgf8_version.argtypes = []
+        L.fgf8_version.restype = ctypes.c_char_p
+        L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, P, I64, P, P, I64, P]
+        L.fp8_quant_w_128x128.argtypes = [P, I64, I64, I64, P, P, I64, P]
+        L.fp8_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, ctypes.c_int, P, I64, ctypes.c_int,
+                                           I64, I64, I64, P, SZ, P]
+        L.fp8_grouped_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, P, I32, P, I64, ctypes.c_int,
+                                                   I64, I64, I64, P, SZ, P]
+        L.fgf8_gemm_workspace_bytes.argtypes = [I64, I64, I64, I32]
+        L.fgf8_gemm_workspace_bytes.restype = SZ
+        L.fgf8_read_status.argtypes = [P, P, ctypes.POINTER(I32)]
+        L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
+        L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
+        for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+                     "fp8_grouped_gemm_blockscaled", "fgf8_read_status", "fgf8_mma_probe",
+                     "fgf8_selftest_wait_timeout"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise FGF8Error(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def round_up(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+_workspaces: dict = {}
+
+
+def workspace_for(device, nbytes: int) -> torch.Tensor:
+    """A zero-filled, 256-byte aligned device workspace of at least nbytes,
+    cached per device (the kernels leave it zeroed for the next call)."""
+    device = torch.device(device)
+    ws = _workspaces.get(device)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
+        assert ws.data_ptr() % 256 == 0
+        _workspaces[device] = ws
+    return ws
+
+
+def fp8_quant_act_1x128(x: torch.Tensor, rows: bool = True, transposed: bool = False):
+    """1x128 activation quantization (and/or the transposed 128x1 output).
+
+    x: BF16 [M, K] CUDA tensor (row stride may exceed K).  Returns
+    (q, s, qT, sT); the ones not requested are None."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    dev = x.device
+    q = s = qT = sT = None
+    if rows:
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s = torch.empty((K // 128, round_up(max(M, 1), 4)), dtype=torch.float32, device=dev)
+    if transposed:
+        qT = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        sT = torch.empty(((M + 127) // 128, round_up(K, 4)), dtype=torch.float32, device=dev)
+    st = lib().fp8_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), _ptr(s),
+                                   s.shape[1] if s is not None else 0, _ptr(qT), _ptr(sT),
+                                   sT.shape[1] if sT is not None else 0, _stream(dev))
+    _check(st, "fp8_quant_act_1x128")
+    return q, s, qT, sT
+
+
+def fp8_quant_w_128x128(w: torch.Tensor):
+    """128x128 weight quantization.  w: BF16 [N, K].  Returns (q, s)."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((K // 128, round_up((N + 127) // 128, 4)), dtype=torch.float32, device=w.device)
+    st = lib().fp8_quant_w_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), _ptr(s), s.shape[1], _stream(w.device))
+    _check(st, "fp8_quant_w_128x128")
+    return q, s
+
+
+def fp8_gemm_blockscaled(A, sa, B, sb, bkind: int = BSCALE_BLOCK128, out_dtype=torch.bfloat16,
+                         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """C = A_hat * B_hat^T.  A [M,K] and B [N,K] uint8 E4M3 codes, sa [K/128, ldsa],
+    sb [K/128, ldsb] float32 (block or per-row kind)."""
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    cdt = OUT_FP32 if out.dtype == torch.float32 else OUT_BF16
+    need = lib().fgf8_gemm_workspace_bytes(M, N, K, 1)
+    ws = workspace if workspace is not None else workspace_for(A.device, need)
+    st = lib().fp8_gemm_blockscaled(_ptr(A), _ptr(sa), sa.stride(0), _ptr(B), _ptr(sb), sb.stride(0), bkind,
+                                    _ptr(out), out.stride(0), cdt, M, N, K, _ptr(ws), ws.numel(),
+                                    _stream(A.device))
+    _check(st, "fp8_gemm_blockscaled")
+    return out
+
+
+def fp8_grouped_gemm_blockscaled(A, sa, B, sb, m_indices, out_dtype=torch.bfloat16,
+                                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Contiguous-layout grouped GEMM.  A [M_total,K], B [E,N,K], sb [E,K/128,ldsb],
+    m_indices int32 [M_total] (-1 = padding row, left unwritten)."""
+    M, K = A.shape
+    E, N, _ = B.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    cdt = OUT_FP32 if out.dtype == torch.float32 else OUT_BF16
+    need = lib().fgf8_gemm_workspace_bytes(M, N, K, E)
+    ws = workspace if workspace is not None else workspace_for(A.device, need)
+    st = lib().fp8_grouped_gemm_blockscaled(_ptr(A), _ptr(sa), sa.stride(0), _ptr(B), _ptr(sb), sb.stride(1),
+                                            _ptr(m_indices), E, _ptr(out), out.stride(0), cdt, M, N, K,
+                                            _ptr(ws), ws.numel(), _stream(A.device))
+    _check(st, "fp8_grouped_gemm_blockscaled")
+    return out
+
+
+def fgf8_mma_probe(A: torch.Tensor, B: torch.Tensor, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Raw tensor-core accumulation of A [128,K] * B [N,K]^T (E4M3 codes), no promotion."""
+    N, K = B.shape
+    D = torch.empty((128, N), dtype=torch.float32, device=A.device)
+    ws = workspace if workspace is not None else workspace_for(A.device, 256)
+    st = lib().fgf8_mma_probe(_ptr(A), _ptr(B), _ptr(D), N, K, _ptr(ws), _stream(A.device))
+    _check(st, "fgf8_mma_probe")
+    return D
+
+
+def fgf8_read_status(workspace: torch.Tensor):
+    """(status, site) of the device status word; resets it.  Synchronizes the stream."""
+    site = ctypes.c_int32(0)
+    st = lib().fgf8_read_status(_ptr(workspace), _stream(workspace.device), ctypes.byref(site))
+    return st, site.value

@@ -1,0 +1,561 @@
+// gemm.cu -- block-scaled FP8 GEMM for sm_103a (tcgen05 + TMA + TMEM).
+//
+// C[m][n] = sum_kb P_kb[m][n] * sa[kb][m] * sb_kb(n),  P_kb = sum_{k in kb} qa*qb
+//
+// "dssusan.co.kr Q&A post 93378" (inner-dimension and E4M3 passages) scales
+// every 128-wide group along K separately, so a K group's partial product
+// must leave the tensor cores before it can be scaled; "kailasan.com
+// recruit post 147436" (hardware-suggestion passage) has the partial results
+// copied out at each interval, multiplied by the scaling factors and added
+// into FP32.  Here that interval is one 128-wide K group:
+//   - warp 0 (one lane) streams A/B tiles and the scale vectors with TMA into
+//     a ring of shared-memory stages;
+//   - warp 1 (one lane) issues 4 tcgen05.mma (K = 32 each) per K group into a
+//     fresh FP32 partial in tensor memory, alternating between two TMEM
+//     buffers so that the next group's MMAs run while this one is promoted;
+//   - warps 4..7 (the promotion warpgroup) read each partial with tcgen05.ld
+//     (one TMEM lane = one output row per thread), multiply by sa*sb and add
+//     into FP32 registers, then write the finished tile (BF16 or FP32).
+// The kernel is persistent: each CTA walks a static list of output tiles.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fgf8 {
+namespace {
+
+constexpr int BM = 128;                 // rows of A per tile (TMEM lanes)
+constexpr int BK = 128;                 // K elements (= bytes) per group
+constexpr int kThreads = 256;           // 8 warps
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kEpiWarp0 = 4;            // warps 4..7: TMEM lane quarters 0..3
+constexpr int kEpiWarps = 4;
+
+// wait-site ids reported in the status word
+enum : int32_t {
+    kSiteProducerEmpty = 1,
+    kSiteProducerScale = 2,
+    kSiteMmaTmemEmpty = 3,
+    kSiteMmaFull = 4,
+    kSiteEpiScale = 5,
+    kSiteEpiTmemFull = 6,
+    kSiteProbe = 7,
+    kSiteSelftest = 99
+};
+
+struct Params {
+    int64_t M, N, K;
+    int32_t KB;
+    int32_t num_m_blocks, num_n_blocks, num_tiles;
+    int32_t m_major;                    // tile order: 1 = m outer, 0 = n outer
+    void *C;
+    int64_t ldc;
+    const int32_t *m_indices;           // grouped layout when non-null
+    int64_t b_rows_per_expert;          // N (grouped)
+    int32_t sb_rows_per_expert;         // KB (grouped)
+    DeviceStatus *status;
+};
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a)
+{
+    return (v + a - 1) / a * a;
+}
+
+template <int BN, int STAGES, int SC, bool ROW_SB>
+struct Layout {
+    static constexpr size_t a_bytes = (size_t)BM * BK;
+    static constexpr size_t b_bytes = (size_t)BN * BK;
+    static constexpr int sb_floats = ROW_SB ? BN : 4;        // floats copied per K group
+    static constexpr int sb_slot = ROW_SB ? BN : 32;         // slot pitch: 128-byte aligned TMA targets
+    static constexpr size_t off_a = 0;
+    static constexpr size_t off_b = off_a + STAGES * a_bytes;
+    static constexpr size_t off_sa = off_b + STAGES * b_bytes;
+    static constexpr size_t off_sb = off_sa + (size_t)SC * BM * 4;
+    static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * sb_slot * 4, 16);
+    static constexpr int num_bars = 2 * STAGES + 2 * SC + 4 + 1;
+    static constexpr size_t off_misc = off_bar + (size_t)num_bars * 8;
+    static constexpr size_t total = off_misc + 16;
+    static constexpr size_t dyn_bytes = total + 1024;    // slack to align the base to 1024
+    static constexpr uint32_t tmem_cols = 2 * BN;        // two partial buffers
+};
+
+__device__ __forceinline__ void tile_coords(int32_t tile, const Params &p, int32_t &mb, int32_t &nb)
+{
+    if (p.m_major) {
+        mb = tile / p.num_n_blocks;
+        nb = tile - mb * p.num_n_blocks;
+    } else {
+        nb = tile / p.num_m_blocks;
+        mb = tile - nb * p.num_m_blocks;
+    }
+}
+
+// Expert of an M block in the grouped layout (-1: padding block, skipped).
+__device__ __forceinline__ int32_t block_expert(const Params &p, int32_t mb)
+{
+    return p.m_indices ? __ldg(p.m_indices + (int64_t)mb * BM) : 0;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float *v)
+{
+    uint4 o;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+    memcpy(&o.x, &h0, 4);
+    memcpy(&o.y, &h1, 4);
+    memcpy(&o.z, &h2, 4);
+    memcpy(&o.w, &h3, 4);
+    *reinterpret_cast<uint4 *>(dst) = o;
+}
+
+template <int BN, int STAGES, int SC, bool ROW_SB, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                            const Params p)
+{
+    using L = Layout<BN, STAGES, SC, ROW_SB>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
+    uint8_t *sm_a = smem + L::off_a;
+    uint8_t *sm_b = smem + L::off_b;
+    float *sm_sa = reinterpret_cast<float *>(smem + L::off_sa);
+    float *sm_sb = reinterpret_cast<float *>(smem + L::off_sb);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *sc_full = bars + 2 * STAGES;
+    uint64_t *sc_empty = bars + 2 * STAGES + SC;
+    uint64_t *tm_full = bars + 2 * STAGES + 2 * SC;
+    uint64_t *tm_empty = tm_full + 2;
+    uint64_t *drain = tm_full + 4;
+    uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::off_misc + 4);
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < SC; ++i) {
+            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tm_full[i], 1);
+            mbar_init(&tm_empty[i], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_base_slot, L::tmem_cols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_base_slot;
+
+    const int32_t KB = p.KB;
+
+    if (warp == kProducerWarp) {
+        if (elect_one()) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            tma_prefetch_desc(&tmSA);
+            tma_prefetch_desc(&tmSB);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+                int32_t mb, nb;
+                tile_coords(tile, p, mb, nb);
+                const int32_t e = block_expert(p, mb);
+                if (e < 0) continue;
+                const int32_t b_row = (int32_t)(e * p.b_rows_per_expert) + nb * BN;
+                const int32_t s_row0 = e * p.sb_rows_per_expert;
+                const int32_t sb_x = ROW_SB ? nb * BN : ((nb * BN / 128) & ~3);
+                for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                        record_timeout(p.status, kSiteProducerEmpty);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(L::a_bytes + L::b_bytes));
+                    tma_load_2d(sm_a + s * L::a_bytes, &tmA, &full[s], kb * BK, mb * BM);
+                    tma_load_2d(sm_b + s * L::b_bytes, &tmB, &full[s], kb * BK, b_row);
+                    const uint32_t j = it % SC, phj = (it / SC) & 1;
+                    if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+                        record_timeout(p.status, kSiteProducerScale);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(BM * 4 + L::sb_floats * 4));
+                    tma_load_2d(sm_sa + j * BM, &tmSA, &sc_full[j], mb * BM, kb);
+                    tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], sb_x, s_row0 + kb);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                // let the copies already issued land before the CTA exits
+                const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0;
+                for (uint32_t i = first; i <= it; ++i)
+                    mbar_wait(&full[i % STAGES], (i / STAGES) & 1, nullptr, 20u * 1000u * 1000u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        const uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            int32_t mb, nb;
+            tile_coords(tile, p, mb, nb);
+            if (block_expert(p, mb) < 0) continue;
+            for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                const uint32_t buf = it & 1, phb = (it >> 1) & 1;
+                if (!mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
+                    record_timeout(p.status, kSiteMmaTmemEmpty);
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(&full[s], ph, abort_flag)) {
+                    record_timeout(p.status, kSiteMmaFull);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                if (elect_one()) {
+                    const uint64_t da = smem_desc_kmajor_sw128(sm_a + s * L::a_bytes);
+                    const uint64_t db = smem_desc_kmajor_sw128(sm_b + s * L::b_bytes);
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)       // 32 bytes = 2 x 16-byte descriptor units
+                        mma_e4m3(d_tmem, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                    mma_commit(&tm_full[buf]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) *abort_flag = 1;
+        // every MMA issued by this warp completes before TMEM is released
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait(drain, 0, nullptr, 20u * 1000u * 1000u);
+    } else if (warp >= kEpiWarp0) {
+        const uint32_t quarter = warp - kEpiWarp0;          // == warp % 4
+        const uint32_t row = quarter * 32 + lane;
+        const uint32_t lane_addr = (quarter * 32) << 16;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            int32_t mb, nb;
+            tile_coords(tile, p, mb, nb);
+            if (block_expert(p, mb) < 0) continue;
+            float acc[BN];
+#pragma unroll
+            for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+            const int sb_sel = ROW_SB ? 0 : ((nb * BN / 128) & 3);
+            for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t j = it % SC, phj = (it / SC) & 1;
+                if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
+                    record_timeout(p.status, kSiteEpiScale);
+                    ok = false;
+                    break;
+                }
+                const float sa_v = sm_sa[j * BM + row];
+                const uint32_t buf = it & 1, phb = (it >> 1) & 1;
+                if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
+                    record_timeout(p.status, kSiteEpiTmemFull);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const float *sbv = sm_sb + j * L::sb_slot;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + c * 32, r);
+                    tmem_ld_wait();
+                    if (ROW_SB) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), sa_v * sbv[c * 32 + i], acc[c * 32 + i]);
+                    } else {
+                        const float scale = sa_v * sbv[sb_sel + (c * 32) / 128];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), scale, acc[c * 32 + i]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&tm_empty[buf]);
+                    mbar_arrive(&sc_empty[j]);
+                }
+            }
+            if (!ok) break;
+            // write the finished row segment
+            const int64_t m = (int64_t)mb * BM + row;
+            bool write = m < p.M;
+            if (write && p.m_indices) write = __ldg(p.m_indices + m) >= 0;
+            if (write) {
+                const int64_t n0 = (int64_t)nb * BN;
+                if (OUT_F32) {
+                    float *dst = static_cast<float *>(p.C) + m * p.ldc + n0;
+#pragma unroll
+                    for (int c = 0; c < BN; c += 4)
+                        if (n0 + c < p.N)
+                            *reinterpret_cast<float4 *>(dst + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                } else {
+                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.C) + m * p.ldc + n0;
+#pragma unroll
+                    for (int c = 0; c < BN; c += 8)
+                        if (n0 + c < p.N) store_row_bf16(dst + c, acc + c);
+                }
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, L::tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------------------
+// Accumulation-precision probe: one CTA, D = A * B^T chained over all of K
+// in one TMEM accumulator (no promotion), raw FP32 written out.
+// ------------------------------------------------------------------------
+constexpr int kProbeMaxN = 256;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mma_probe_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float *D, int N,
+                     int K, DeviceStatus *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
+    uint8_t *sm_a = smem;                         // 16 KB
+    uint8_t *sm_b = smem + BM * BK;               // up to 32 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BM * BK + kProbeMaxN * BK);
+    uint64_t *full = bars, *done = bars + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    const uint32_t warp = warp_id(), lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        mbar_init(full, 1);
+        mbar_init(done, 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, kProbeMaxN);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    __shared__ int ok_all;
+    if (threadIdx.x == 0) ok_all = 1;
+    __syncthreads();
+
+    const int KB = K / BK;
+    for (int kb = 0; kb < KB; ++kb) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(full, (uint32_t)(BM * BK + N * BK));
+            tma_load_2d(sm_a, &tmA, full, kb * BK, 0);
+            tma_load_2d(sm_b, &tmB, full, kb * BK, 0);
+        }
+        if (warp == kMmaWarp) {
+            bool ok = mbar_wait(full, kb & 1, nullptr);
+            if (ok) {
+                tc_fence_after_sync();
+                if (elect_one()) {
+                    const uint64_t da = smem_desc_kmajor_sw128(sm_a);
+                    const uint64_t db = smem_desc_kmajor_sw128(sm_b);
+                    const uint32_t idesc = idesc_e4m3_f32(BM, N);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) mma_e4m3(tmem, da + 2 * k, db + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(done);
+                }
+                __syncwarp();
+                ok = mbar_wait(done, kb & 1, nullptr);
+            }
+            if (!ok && lane == 0) {
+                record_timeout(status, kSiteProbe);
+                ok_all = 0;
+            }
+        }
+        __syncthreads();                 // stage buffers are reused next iteration
+        if (!ok_all) break;
+    }
+    if (warp >= kEpiWarp0 && ok_all) {
+        tc_fence_after_sync();
+        const uint32_t quarter = warp - kEpiWarp0;
+        const uint32_t row = quarter * 32 + lane;
+        for (int c = 0; c < N; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem + ((quarter * 32) << 16) + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (c + i < N) D[(int64_t)row * N + c + i] = __uint_as_float(r[i]);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kProbeMaxN);
+    }
+}
+
+// A wait on a barrier that nothing arrives on: exercises the bounded-wait
+// path (status word set, TMEM released, kernel returns) without any fault.
+__global__ void wait_timeout_selftest_kernel(DeviceStatus *status, uint64_t budget_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_slot;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    tmem_alloc(&tmem_slot, 32);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const bool ok = mbar_wait(&bar, 0, nullptr, budget_ns);
+    if (!ok && threadIdx.x == 0) record_timeout(status, kSiteSelftest);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_slot, 32);
+}
+
+// ------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+template <int BN, int STAGES, int SC, bool ROW_SB, bool OUT_F32>
+cudaError_t launch_variant(const GemmArgs &a, const Params &p, int grid, cudaStream_t stream)
+{
+    using L = Layout<BN, STAGES, SC, ROW_SB>;
+    CUtensorMap tmA, tmB, tmSA, tmSB;
+    const int64_t KB = a.K / BK;
+    const int64_t b_rows = a.m_indices ? (int64_t)a.num_experts * a.N : a.N;
+    const int64_t sb_rows = a.m_indices ? (int64_t)a.num_experts * KB : KB;
+    if (!make_tensor_map_2d(&tmA, 1, false, a.A, a.K, a.M, a.K, BK, BM, true) ||
+        !make_tensor_map_2d(&tmB, 1, false, a.B, a.K, b_rows, a.K, BK, BN, true) ||
+        !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, KB, a.ldsa * 4, BM, 1, false) ||
+        !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, sb_rows, a.ldsb * 4, L::sb_floats, 1, false))
+        return cudaErrorInvalidValue;
+    auto kern = gemm_blockscaled_kernel<BN, STAGES, SC, ROW_SB, OUT_F32>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kThreads, L::dyn_bytes, stream>>>(tmA, tmB, tmSA, tmSB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool make_tensor_map_2d(void *map, int dtype_bytes, bool is_float, const void *base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const CUtensorMapDataType dt =
+        dtype_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : (is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32);
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(reinterpret_cast<CUtensorMap *>(map), dt, 2, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t gemm_workspace_bytes(int64_t, int64_t, int64_t, int32_t, int)
+{
+    return kWsHeaderBytes;
+}
+
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    constexpr int BN = 128;
+    Params p{};
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.KB = (int32_t)(a.K / BK);
+    p.num_m_blocks = (int32_t)((a.M + BM - 1) / BM);
+    p.num_n_blocks = (int32_t)((a.N + BN - 1) / BN);
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.m_major = a.m_indices != nullptr ? 1 : 0;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.m_indices = a.m_indices;
+    p.b_rows_per_expert = a.m_indices ? a.N : 0;
+    p.sb_rows_per_expert = a.m_indices ? p.KB : 0;
+    p.status = reinterpret_cast<DeviceStatus *>(a.workspace);
+    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    if (a.bkind == 1) {
+        return a.out_f32 ? launch_variant<BN, 6, 8, true, true>(a, p, grid, stream)
+                         : launch_variant<BN, 6, 8, true, false>(a, p, grid, stream);
+    }
+    return a.out_f32 ? launch_variant<BN, 6, 8, false, true>(a, p, grid, stream)
+                     : launch_variant<BN, 6, 8, false, false>(a, p, grid, stream);
+}
+
+cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,
+                             cudaStream_t stream)
+{
+    CUtensorMap tmA, tmB;
+    if (!make_tensor_map_2d(&tmA, 1, false, A, K, BM, K, BK, BM, true) ||
+        !make_tensor_map_2d(&tmB, 1, false, B, K, N, K, BK, N, true))
+        return cudaErrorInvalidValue;
+    const size_t smem = 1024 + BM * BK + kProbeMaxN * BK + 64;
+    cudaError_t err = cudaFuncSetAttribute(mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    mma_probe_kernel<<<1, kThreads, smem, stream>>>(tmA, tmB, D, N, K, reinterpret_cast<DeviceStatus *>(workspace));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(void *workspace, uint32_t budget_us, cudaStream_t stream)
+{
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<DeviceStatus *>(workspace),
+                                                      (uint64_t)budget_us * 1000ull);
+    return cudaGetLastError();
+}
+
+}  // namespace fgf8

@@ -1,0 +1,50 @@
+// kernels.h -- launchers shared between the kernel files and the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace fgf8 {
+
+cudaError_t launch_quant_act_rows(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
+                                  int64_t lds, cudaStream_t stream);
+cudaError_t launch_quant_act_tiles(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
+                                   int64_t lds, uint8_t *qT, float *sT, int64_t ldsT, cudaStream_t stream);
+cudaError_t launch_quant_w(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, float *s, int64_t lds,
+                           cudaStream_t stream);
+
+struct GemmArgs {
+    const uint8_t *A;
+    const float *sa;
+    int64_t ldsa;
+    const uint8_t *B;
+    const float *sb;
+    int64_t ldsb;
+    int bkind;              // 0: 128x128 block scales, 1: per-row scales
+    void *C;
+    int64_t ldc;
+    int out_f32;            // 0: BF16 output, 1: FP32 output
+    int64_t M, N, K;
+    const int32_t *m_indices;   // grouped contiguous layout when non-null
+    int32_t num_experts;
+    void *workspace;
+    size_t ws_bytes;
+};
+
+// Workspace layout: [0, 256) status word; split-K partials and counters after.
+constexpr size_t kWsHeaderBytes = 256;
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int num_sms);
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
+cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,
+                             cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(void *workspace, uint32_t budget_us, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).  Returns false if the driver rejects the map.
+bool make_tensor_map_2d(void *map, int dtype_bytes, bool is_float, const void *base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+
+}  // namespace fgf8

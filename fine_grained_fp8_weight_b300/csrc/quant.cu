@@ -1,0 +1,283 @@
+// quant.cu -- fine-grained E4M3 quantization kernels for sm_103a.
+//
+// Rule ("dssusan.co.kr Q&A post 93378", Figure 7(a) passage: 1x128 tiles for
+// activations, 128x128 blocks for weights, each scaled by its own max-abs):
+//   amax = max |x| over the group,  s = amax / 448 (binary32 division),
+//   q = E4M3_rn_satfinite(fl32(x / s)),  s == 0 -> q = signed zero.
+// Every kernel here is HBM-bound: it reads 2 bytes and writes 1 byte (plus
+// 4/128 or 4/16384 bytes of scale) per element, once.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace fgf8 {
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+
+// Two binary32 values to two E4M3 codes (round to nearest even, saturate to
+// +-448); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// x / s with IEEE round-to-nearest; s == 0 only for an all-zero group, whose
+// elements are +-0 and encode to signed zeros directly.
+__device__ __forceinline__ float scaled(float x, float s)
+{
+    return s == 0.0f ? x : __fdiv_rn(x, s);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s)
+{
+    uint2 o;
+    o.x = cvt_e4m3x2(scaled(f[0], s), scaled(f[1], s)) | (cvt_e4m3x2(scaled(f[2], s), scaled(f[3], s)) << 16);
+    o.y = cvt_e4m3x2(scaled(f[4], s), scaled(f[5], s)) | (cvt_e4m3x2(scaled(f[6], s), scaled(f[7], s)) << 16);
+    return o;
+}
+
+__device__ __forceinline__ float amax8(const float (&f)[8])
+{
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
+    return a;
+}
+
+// ------------------------------------------------------------------------
+// 1x128 tiles along K.  A half-warp (16 lanes x 8 BF16) covers one tile; a
+// warp covers two consecutive tiles per round and kRounds rounds, with all
+// loads issued before any arithmetic so that enough bytes are in flight.
+// ------------------------------------------------------------------------
+constexpr int kActRounds = 4;
+constexpr int kActWarps = 8;
+
+__global__ void __launch_bounds__(kActWarps * 32)
+    quant_act_rows_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t KB, int64_t ldx,
+                          uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds)
+{
+    const int64_t total = M * KB;
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4;
+    const int sub = lane & 15;
+    const int64_t warp_global = (int64_t)blockIdx.x * kActWarps + (threadIdx.x >> 5);
+    const int64_t first = warp_global * (2 * kActRounds);
+
+    uint4 raw[kActRounds];
+    int64_t mrow[kActRounds], kblk[kActRounds];
+#pragma unroll
+    for (int r = 0; r < kActRounds; ++r) {
+        const int64_t t = first + 2 * r + half;
+        mrow[r] = -1;
+        raw[r] = make_uint4(0, 0, 0, 0);
+        if (t < total) {
+            mrow[r] = t / KB;
+            kblk[r] = t - mrow[r] * KB;
+            const __nv_bfloat16 *src = x + mrow[r] * ldx + kblk[r] * 128 + sub * 8;
+            raw[r] = __ldcs(reinterpret_cast<const uint4 *>(src));
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kActRounds; ++r) {
+        float f[8];
+        bf16x8_to_f32(raw[r], f);
+        float a = amax8(f);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (mrow[r] >= 0) {
+            const float sc = __fdiv_rn(a, kE4M3Max);
+            const uint2 codes = encode8(f, sc);
+            const int64_t K = KB * 128;
+            *reinterpret_cast<uint2 *>(q + mrow[r] * K + kblk[r] * 128 + sub * 8) = codes;
+            if (sub == 0) s[kblk[r] * lds + mrow[r]] = sc;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
+// 128 tokens x 128 channels per CTA, staged in shared memory: the column
+// (token-direction, 128x1) groups give the transposed output qT/sT; when q/s
+// are requested too, the row (1x128) groups of the same tile are encoded
+// from the same staged data.  M % 16 == 0 when qT is written.
+// ------------------------------------------------------------------------
+constexpr int kTileThreads = 256;
+constexpr int kTilePitch = 128 + 8;   // BF16 elements per staged row (pad breaks bank conflicts)
+
+__global__ void __launch_bounds__(kTileThreads)
+    quant_act_tile_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                          uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds,
+                          uint8_t *__restrict__ qT, float *__restrict__ sT, int64_t ldsT)
+{
+    __shared__ __align__(16) __nv_bfloat16 tile[128 * kTilePitch];
+    __shared__ float part[2][128];
+
+    const int64_t kb = blockIdx.x;          // channel group
+    const int64_t tb = blockIdx.y;          // token group
+    const int64_t m0 = tb * 128;
+    const int rows = (int)((M - m0) < 128 ? (M - m0) : 128);
+    const int tid = threadIdx.x;
+
+    // stage: 128 rows x 256 bytes = 2048 chunks of 16 bytes, 8 per thread
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = tid + i * kTileThreads;
+        const int r = c >> 4, c16 = c & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < rows) v = __ldcs(reinterpret_cast<const uint4 *>(x + (m0 + r) * ldx + kb * 128 + c16 * 8));
+        *reinterpret_cast<uint4 *>(&tile[r * kTilePitch + c16 * 8]) = v;
+    }
+    __syncthreads();
+
+    if (qT != nullptr) {
+        // two threads per channel, 64 tokens each
+        const int ch = tid & 127;
+        const int h = tid >> 7;
+        float a = 0.0f;
+        for (int r = h * 64; r < h * 64 + 64; ++r) a = fmaxf(a, fabsf(__bfloat162float(tile[r * kTilePitch + ch])));
+        part[h][ch] = a;
+        __syncthreads();
+        const float amax = fmaxf(part[0][ch], part[1][ch]);
+        const float sc = __fdiv_rn(amax, kE4M3Max);
+        if (h == 0) sT[tb * ldsT + kb * 128 + ch] = sc;
+        // encode this thread's 64 tokens of channel ch into qT[kb*128+ch][m0 + h*64 ...]
+        uint8_t *dst = qT + (kb * 128 + ch) * M + m0 + h * 64;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int r0 = h * 64 + g * 16;
+            if (r0 >= rows) break;          // rows is a multiple of 16 here
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float f0 = __bfloat162float(tile[(r0 + 4 * j + 0) * kTilePitch + ch]);
+                float f1 = __bfloat162float(tile[(r0 + 4 * j + 1) * kTilePitch + ch]);
+                float f2 = __bfloat162float(tile[(r0 + 4 * j + 2) * kTilePitch + ch]);
+                float f3 = __bfloat162float(tile[(r0 + 4 * j + 3) * kTilePitch + ch]);
+                w[j] = cvt_e4m3x2(scaled(f0, sc), scaled(f1, sc)) | (cvt_e4m3x2(scaled(f2, sc), scaled(f3, sc)) << 16);
+            }
+            *reinterpret_cast<uint4 *>(dst + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+
+    if (q != nullptr) {
+        // row groups: 16 lanes per token row, 8 channels per lane
+        const int lane = tid & 31, sub = lane & 15;
+        const int row_in_pass = (tid >> 4);          // 0..15
+        for (int r = row_in_pass; r < rows; r += kTileThreads / 16) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r * kTilePitch + sub * 8]);
+            float f[8];
+            bf16x8_to_f32(v, f);
+            float a = amax8(f);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float sc = __fdiv_rn(a, kE4M3Max);
+            *reinterpret_cast<uint2 *>(q + (m0 + r) * K + kb * 128 + sub * 8) = encode8(f, sc);
+            if (sub == 0) s[kb * lds + m0 + r] = sc;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
+// 128x128 weight blocks: one CTA per block, the block held in registers
+// (8 x 16 bytes per thread) across the max-abs reduction and the encode.
+// ------------------------------------------------------------------------
+constexpr int kBlockThreads = 256;
+
+__global__ void __launch_bounds__(kBlockThreads)
+    quant_w_block_kernel(const __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                         uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds)
+{
+    __shared__ float red[kBlockThreads / 32];
+    const int64_t kb = blockIdx.x;
+    const int64_t nb = blockIdx.y;
+    const int64_t n0 = nb * 128;
+    const int rows = (int)((N - n0) < 128 ? (N - n0) : 128);
+    const int tid = threadIdx.x;
+
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = tid + i * kBlockThreads;
+        const int r = c >> 4, c16 = c & 15;
+        raw[i] = make_uint4(0, 0, 0, 0);
+        if (r < rows) raw[i] = __ldcs(reinterpret_cast<const uint4 *>(w + (n0 + r) * ldw + kb * 128 + c16 * 8));
+    }
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        bf16x8_to_f32(raw[i], f);
+        a = fmaxf(a, amax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((tid & 31) == 0) red[tid >> 5] = a;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kBlockThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    const float sc = __fdiv_rn(amax, kE4M3Max);
+    if (tid == 0) s[kb * lds + nb] = sc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = tid + i * kBlockThreads;
+        const int r = c >> 4, c16 = c & 15;
+        if (r < rows) {
+            float f[8];
+            bf16x8_to_f32(raw[i], f);
+            *reinterpret_cast<uint2 *>(q + (n0 + r) * K + kb * 128 + c16 * 8) = encode8(f, sc);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act_rows(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
+                                  int64_t lds, cudaStream_t stream)
+{
+    const int64_t KB = K / 128;
+    const int64_t tiles = M * KB;
+    const int64_t per_block = (int64_t)kActWarps * 2 * kActRounds;
+    const int64_t blocks = (tiles + per_block - 1) / per_block;
+    if (blocks == 0) return cudaSuccess;
+    quant_act_rows_kernel<<<(unsigned)blocks, kActWarps * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(x), M, KB, ldx, q, s, lds);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_tiles(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
+                                   int64_t lds, uint8_t *qT, float *sT, int64_t ldsT, cudaStream_t stream)
+{
+    const dim3 grid((unsigned)(K / 128), (unsigned)((M + 127) / 128));
+    if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+    quant_act_tile_kernel<<<grid, kTileThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), M, K, ldx, q,
+                                                             s, lds, qT, sT, ldsT);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_w(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, float *s, int64_t lds,
+                           cudaStream_t stream)
+{
+    const dim3 grid((unsigned)(K / 128), (unsigned)((N + 127) / 128));
+    if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+    quant_w_block_kernel<<<grid, kBlockThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), N, K, ldw, q, s,
+                                                             lds);
+    return cudaGetLastError();
+}
+
+}  // namespace fgf8

@@ -82,14 +82,15 @@ const char *fgf8_version(void);
  * division); q = E4M3(fl32(x / s)) with round-to-nearest-even and saturation
  * to +-448; an all-zero group gives s = 0 and signed zeros.
  *
- *   x   : BF16 [M][ldx], ldx >= K.  K % 128 == 0.  M >= 0 (M == 0: no-op).
+ *   x   : BF16 [M][ldx], ldx >= K.  K % 128 == 0.  M >= 0; M == 0 is a no-op
+ *         that reads no pointer (they may be NULL).
  *   q   : E4M3 [M][K] (row stride K), groups along K;           may be NULL
  *   s   : float [K/128][lds], s[kb*lds + m]; lds >= M, lds % 4 == 0;  NULL iff q is
  *   qT  : E4M3 [K][M] (row stride M), groups of 128 tokens along M (the last
  *         group may be partial: amax over the tokens present);       may be NULL
  *   sT  : float [ceil(M/128)][ldsT], sT[tb*ldsT + k]; ldsT >= K, ldsT % 4 == 0; NULL iff qT is
- * At least one of q, qT must be given.  x must be 8-byte aligned with ldx % 4
- * == 0; q, s, qT, sT 16-byte aligned; with qT given, M % 16 == 0.
+ * At least one of q, qT must be given.  x must be 16-byte aligned with
+ * ldx % 8 == 0; q, s, qT, sT 16-byte aligned; with qT given, M % 16 == 0.
  */
 fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
                                 uint8_t *q, float *s, int64_t lds,
@@ -100,9 +101,9 @@ fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx
  * fp8_quant_w_128x128 -- weight quantization in 128x128 blocks (per 128 input
  * channels per 128 output channels), [dssusan] Figure 7(a) passage.  Same rule
  * as above with amax over the block; a ragged last block row (N % 128 != 0)
- * takes amax over the rows present.
+ * takes amax over the rows present.  N == 0 is a no-op that reads no pointer.
  *
- *   w : BF16 [N][ldw], ldw >= K, ldw % 4 == 0, 8-byte aligned.  K % 128 == 0.
+ *   w : BF16 [N][ldw], ldw >= K, ldw % 8 == 0, 16-byte aligned.  K % 128 == 0.
  *   q : E4M3 [N][K], 16-byte aligned.
  *   s : float [K/128][lds], s[kb*lds + nb]; lds >= ceil(N/128), lds % 4 == 0.
  */

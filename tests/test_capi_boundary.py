@@ -1,0 +1,117 @@
+"""The C-ABI library loads, exports every function the headers declare, and
+rejects bad arguments on the host with the documented status codes (these
+checks run before any device call, so no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fine_grained_fp8_weight_b300 as fg
+from fine_grained_fp8_weight_b300 import build as fgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fgbuild.build()
+    return fg.lib()
+
+
+def _declared():
+    names = set()
+    for h in ("fgf8.h", "fgf8_testing.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b((?:fp8|fgf8)_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared()
+    assert declared == set(fg.EXPORTED)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert L.fgf8_status_string(code)
+    assert L.fgf8_version().startswith(b"fgf8")
+
+
+# fake, never-dereferenced device addresses
+A16 = ctypes.c_void_p(0x10000)
+MIS = ctypes.c_void_p(0x10008)
+
+
+def test_quant_act_rejects(L):
+    f = L.fp8_quant_act_1x128
+    assert f(None, 4, 128, 128, A16, A16, 4, None, None, 0, None) == 1         # null x
+    assert f(A16, 4, 128, 128, None, None, 0, None, None, 0, None) == 1      # no output
+    assert f(A16, 4, 128, 128, A16, None, 4, None, None, 0, None) == 1       # q without s
+    assert f(A16, 4, 100, 100, A16, A16, 4, None, None, 0, None) == 3        # K % 128
+    assert f(A16, 4, 128, 128, A16, A16, 2, None, None, 0, None) == 1        # lds < M
+    assert f(A16, 4, 128, 128, A16, A16, 6, None, None, 0, None) == 1        # lds % 4
+    assert f(MIS, 4, 128, 128, A16, A16, 4, None, None, 0, None) == 2        # x misaligned
+    assert f(A16, 4, 128, 132, A16, A16, 4, None, None, 0, None) == 2        # ldx % 8
+    assert f(A16, 20, 128, 128, None, None, 0, A16, A16, 128, None) == 3     # qT needs M % 16
+    assert f(A16, 16, 128, 128, None, None, 0, A16, A16, 126, None) == 1     # ldsT < K
+
+
+def test_quant_w_rejects(L):
+    f = L.fp8_quant_w_128x128
+    assert f(None, 128, 128, 128, A16, A16, 4, None) == 1
+    assert f(A16, 128, 200, 200, A16, A16, 4, None) == 3
+    assert f(A16, 300, 128, 128, A16, A16, 2, None) == 1                     # lds < ceil(N/128)
+    assert f(A16, 128, 128, 128, MIS, A16, 4, None) == 2
+
+
+def test_gemm_rejects(L):
+    f = L.fp8_gemm_blockscaled
+    ok = dict(A=A16, sa=A16, ldsa=4, B=A16, sb=A16, ldsb=4, bk=0, C=A16, ldc=128, cdt=0,
+              M=4, N=128, K=128, ws=A16, wsb=1 << 20, st=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["A"], a["sa"], a["ldsa"], a["B"], a["sb"], a["ldsb"], a["bk"], a["C"], a["ldc"], a["cdt"],
+                 a["M"], a["N"], a["K"], a["ws"], a["wsb"], a["st"])
+
+    assert call(A=None) == 1
+    assert call(ws=None) == 1
+    assert call(M=0) == 1
+    assert call(bk=5) == 1
+    assert call(cdt=3) == 1
+    assert call(K=200) == 3
+    assert call(N=120, ldc=120) == 3
+    assert call(ldsa=2) == 1
+    assert call(bk=1, ldsb=64) == 1          # per-row scales need ldsb >= N
+    assert call(ldc=100) == 1
+    assert call(B=MIS) == 2
+    assert call(ldc=132) == 2                # 264-byte rows are not 16-byte multiples
+    assert call(ws=ctypes.c_void_p(0x10010)) == 2
+    assert call(wsb=16) == 5
+
+
+def test_grouped_rejects(L):
+    f = L.fp8_grouped_gemm_blockscaled
+    base = [A16, A16, 256, A16, A16, 4, A16, 2, A16, 128, 0, 256, 128, 128, A16, 1 << 20, None]
+    bad = list(base); bad[6] = None
+    assert f(*bad) == 1                      # no m_indices
+    bad = list(base); bad[11] = 200
+    assert f(*bad) == 3                      # M_total % 128
+    bad = list(base); bad[7] = 0
+    assert f(*bad) == 1                      # no experts
+
+
+def test_probe_rejects(L):
+    f = L.fgf8_mma_probe
+    assert f(A16, A16, A16, 24, 128, A16, None) == 3
+    assert f(A16, A16, A16, 512, 128, A16, None) == 3
+    assert f(A16, A16, A16, 32, 100, A16, None) == 3
+    assert f(None, A16, A16, 32, 128, A16, None) == 1
+
+
+def test_workspace_size(L):
+    assert L.fgf8_gemm_workspace_bytes(4096, 18432, 7168, 1) >= 256

@@ -1,0 +1,156 @@
+"""GPU parity of the block-scaled FP8 GEMM (dense, per-row B scales, grouped):
+every output element within |C - C_ref| <= 2^-7 * sum|a_hat*b_hat| + 1e-6 of
+the oracle's binary64 result, through the C ABI, on seeded inputs.  The
+quantized operands come from the oracle, so the GEMM is tested on its own."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fine_grained_fp8_weight_b300 as fg
+from fine_grained_fp8_weight_b300 import workloads as wl
+from tests.gpu_util import DEV, assert_within_bound, bf16_out_to_f64, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _d(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _run_dense(Abits, Bbits, out_dtype, rows=None, bkind=0):
+    qa, sa = oracle.quant_act_1x128(Abits)
+    if bkind == 0:
+        qb, sb = oracle.quant_w_128x128(Bbits)
+    else:
+        qb, sb = oracle.quant_act_1x128(Bbits)          # per-row (1x128) B scales
+    C = fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), bkind=bkind, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    Cg = bf16_out_to_f64(C) if out_dtype == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb, bkind, rows=rows)
+    if rows is not None:
+        Cg = Cg[rows]
+    return Cg, Cr, S
+
+
+def test_tiny_workload():
+    g = wl.tiny().gemms[0]
+    Cg, Cr, S = _run_dense(g.A, g.B, torch.bfloat16)
+    mx, mean = assert_within_bound(Cg, Cr, S, "tiny")
+    assert mx < 2.0 ** -7
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (1, 16, 128), (77, 144, 256), (300, 400, 512),
+                                   (256, 256, 1024), (129, 272, 384), (1000, 48, 128)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_dense_shapes(M, N, K, out):
+    rng = np.random.default_rng(M * 31 + N * 7 + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (N, K), 0.02)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    Cg, Cr, S = _run_dense(A, B, dt)
+    assert_within_bound(Cg, Cr, S, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 256, 512), (256, 144, 384)])
+def test_row_scaled_b(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.001, 50.0)
+    B = wl.bf16_normal(rng, (N, K), 1.0, 0.001, 50.0)
+    Cg, Cr, S = _run_dense(A, B, torch.float32, bkind=1)
+    assert_within_bound(Cg, Cr, S, "row-scaled")
+
+
+def test_fp32_fp32_accumulation_is_tight():
+    # with FP32 output the error comes only from the tensor-core partial sums
+    # and the FP32 promotion: far below the stated bound
+    rng = np.random.default_rng(3)
+    A = wl.bf16_normal(rng, (256, 2048), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (256, 2048), 0.02)
+    Cg, Cr, S = _run_dense(A, B, torch.float32)
+    mx, _ = assert_within_bound(Cg, Cr, S)
+    assert mx < 2.0 ** -16
+
+
+def test_zero_operand_gives_zero():
+    A = np.zeros((128, 256), np.uint16)
+    B = wl.bf16_normal(np.random.default_rng(4), (128, 256), 0.02)
+    Cg, Cr, S = _run_dense(A, B, torch.bfloat16)
+    assert np.all(Cg == 0)
+
+
+def test_output_row_stride_and_untouched_padding():
+    rng = np.random.default_rng(6)
+    A = wl.bf16_normal(rng, (130, 256))
+    B = wl.bf16_normal(rng, (48, 256), 0.02)
+    qa, sa = oracle.quant_act_1x128(A)
+    qb, sb = oracle.quant_w_128x128(B)
+    big = torch.full((130, 64), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = big[:, :48]
+    fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:, 48:]).all(), "columns past N were written"
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb)
+    assert_within_bound(bf16_out_to_f64(out), Cr, S)
+
+
+def _grouped_case(seed, counts, N, K, rows=None):
+    w = wl.grouped_small(seed, counts, N, K).gemms[0]
+    qa, sa = oracle.quant_act_1x128(w.A)
+    E = w.B.shape[0]
+    qbs, sbs = zip(*[oracle.quant_w_128x128(w.B[e]) for e in range(E)])
+    qb = np.stack(qbs)
+    sb = np.stack(sbs)
+    out = torch.full((w.A.shape[0], N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    fg.fp8_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), _d(w.m_indices), out=out)
+    torch.cuda.synchronize()
+    Cr, S = oracle.grouped_gemm_blockscaled(qa, sa, qb, sb, w.m_indices, rows=rows)
+    Cg = bf16_out_to_f64(out)
+    if rows is not None:
+        Cg = Cg[rows]
+    return w, Cg, Cr, S
+
+
+@pytest.mark.parametrize("counts", [[130, 0, 70, 256], [1], [0, 0, 300], [128, 128]])
+def test_grouped_small(counts):
+    w, Cg, Cr, S = _grouped_case(sum(counts) + len(counts), counts, 144, 256)
+    real = w.m_indices >= 0
+    assert_within_bound(Cg[real], Cr[real], S[real], "grouped")
+    assert np.all(np.isnan(Cg[~real])), "padding rows were written"
+
+
+# --- full-size workloads, sampled rows ---
+
+def _sample_rows(M, n, seed):
+    return np.sort(np.random.default_rng(seed).choice(M, size=min(n, M), replace=False))
+
+
+def test_full_size_prefill_pair_sampled():
+    for g, seed in zip(wl.prefill_pair().gemms, (11, 12)):
+        rows = _sample_rows(g.A.shape[0], 3, seed)
+        Cg, Cr, S = _run_dense(g.A, g.B, torch.bfloat16, rows=rows)
+        assert_within_bound(Cg, Cr, S, g.name)
+
+
+def test_full_size_decode():
+    for g in wl.decode().gemms:
+        rows = _sample_rows(g.A.shape[0], 8, 13)
+        Cg, Cr, S = _run_dense(g.A, g.B, torch.bfloat16, rows=rows)
+        assert_within_bound(Cg, Cr, S, g.name)
+
+
+def test_full_size_wgrad_sampled():
+    g = wl.wgrad().gemms[0]
+    dYt, sdY = oracle.quant_act_128x1(g.dY)       # [N, T], [T/128, N]
+    Xt, sX = oracle.quant_act_128x1(g.X)          # [K, T], [T/128, K]
+    C = fg.fp8_gemm_blockscaled(_d(dYt), _d(sdY), _d(Xt), _d(sX), bkind=fg.BSCALE_ROW1x128,
+                                out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rows = _sample_rows(dYt.shape[0], 3, 14)
+    Cr, S = oracle.gemm_blockscaled(dYt, sdY, Xt, sX, 1, rows=rows)
+    assert_within_bound(C.cpu().numpy().astype(np.float64)[rows], Cr, S, "wgrad")
