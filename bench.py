@@ -1,0 +1,452 @@
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+One step = the whole path over the prefill projection pair (GEMM1 4096 x
+18432 x 7168, GEMM2 4096 x 7168 x 18432, BF16 output):
+
+    quantize A1 (1x128) -> quantize W1 (128x128) -> block-scaled GEMM1 ->
+    quantize A2 (1x128) -> quantize W2 (128x128) -> block-scaled GEMM2
+
+``value`` is the step's GEMM FLOPs (2*M*N*K summed over both GEMMs) divided by
+the device time of the step, with all inputs resident in HBM (BF16 inputs of
+738 MB per step, larger than the 126 MB L2, so no flush is needed between
+steps).  The JSON line also carries the roofline of the dominant kernel (the
+GEMM), per-kernel times, quantize bandwidth, an end-to-end figure through the
+public API with pinned host buffers, and the CPU oracle timed on a bounded
+sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload prefill|decode|moe|wgrad|tiny] [--profile-gemm]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% of FP8 peak); quantize GB/s (% of HBM)"
+FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            t = time.time()
+            while not self.lines and time.time() - t < 5.0:     # first sample before timing starts
+                time.sleep(0.02)
+            self.lines.clear()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------- workloads --
+
+def make_workload(name):
+    from fine_grained_fp8_weight_b300 import workloads as wl
+    if name == "prefill":
+        return wl.prefill_pair()
+    if name == "decode":
+        return wl.decode()
+    if name == "moe":
+        return wl.moe_grouped()
+    if name == "wgrad":
+        return wl.wgrad()
+    if name == "tiny":
+        return wl.tiny()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def gemm_flops(g):
+    from fine_grained_fp8_weight_b300.workloads import Dense, Grouped, Wgrad
+    if isinstance(g, Dense):
+        return 2.0 * g.A.shape[0] * g.B.shape[0] * g.A.shape[1]
+    if isinstance(g, Grouped):
+        return 2.0 * float(g.counts.sum()) * g.B.shape[1] * g.A.shape[1]
+    if isinstance(g, Wgrad):
+        return 2.0 * g.dY.shape[1] * g.X.shape[1] * g.dY.shape[0]
+    raise TypeError(g)
+
+
+class DevicePath:
+    """The step on device buffers: every op is one C-ABI call on one stream."""
+
+    def __init__(self, work, dev):
+        import torch
+        import fine_grained_fp8_weight_b300 as fg
+        from fine_grained_fp8_weight_b300 import workloads as wl
+        from fine_grained_fp8_weight_b300.workloads import Dense, Grouped, Wgrad
+        self.fg, self.torch, self.dev = fg, torch, dev
+        self.ops = []          # (kind, name, callable, bytes or flops)
+        self.inputs = []       # (host numpy bits, device tensor) for the end-to-end leg
+        self.outputs = []
+        for g in work.gemms:
+            if isinstance(g, Dense):
+                A = wl.bf16_bits_to_torch(g.A).to(dev)
+                B = wl.bf16_bits_to_torch(g.B).to(dev)
+                self.inputs += [(g.A, A), (g.B, B)]
+                M, K = A.shape
+                N = B.shape[0]
+                st = {}
+                C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                self.outputs.append(C)
+                qbytes = lambda r, c, sc: r * c * 3 + sc * 4
+                self.ops.append(("quant", f"{g.name}.quant_act_1x128",
+                                 lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)),
+                                 qbytes(M, K, M * K // 128)))
+                self.ops.append(("quant", f"{g.name}.quant_w_128x128",
+                                 lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128(B)),
+                                 qbytes(N, K, (N // 128 + 1) * K // 128)))
+                self.ops.append(("gemm", f"{g.name}.gemm",
+                                 lambda st=st, C=C: fg.fp8_gemm_blockscaled(st["a"][0], st["a"][1], st["b"][0],
+                                                                            st["b"][1], out=C),
+                                 gemm_flops(g)))
+            elif isinstance(g, Grouped):
+                A = wl.bf16_bits_to_torch(g.A).to(dev)
+                B = wl.bf16_bits_to_torch(g.B).to(dev)
+                mi = torch.from_numpy(g.m_indices).to(dev)
+                self.inputs += [(g.A, A), (g.B, B)]
+                M, K = A.shape
+                E, N, _ = B.shape
+                st = {}
+                C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                self.outputs.append(C)
+                self.ops.append(("quant", f"{g.name}.quant_act_1x128",
+                                 lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)), M * K * 3 + M * K // 32))
+                self.ops.append(("quant", f"{g.name}.quant_w_128x128_grouped",
+                                 lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128_grouped(B)), E * N * K * 3))
+                self.ops.append(("gemm", f"{g.name}.grouped_gemm",
+                                 lambda st=st, C=C, mi=mi: fg.fp8_grouped_gemm_blockscaled(
+                                     st["a"][0], st["a"][1], st["b"][0], st["b"][1], mi, out=C),
+                                 gemm_flops(g)))
+            elif isinstance(g, Wgrad):
+                dY = wl.bf16_bits_to_torch(g.dY).to(dev)
+                X = wl.bf16_bits_to_torch(g.X).to(dev)
+                self.inputs += [(g.dY, dY), (g.X, X)]
+                T, N = dY.shape
+                K = X.shape[1]
+                st = {}
+                C = torch.empty((N, K), dtype=torch.float32, device=dev)
+                self.outputs.append(C)
+                self.ops.append(("quant", f"{g.name}.quant_dY_128x1",
+                                 lambda dY=dY, st=st: st.update(a=fg.fp8_quant_act_1x128(dY, rows=False, transposed=True)),
+                                 T * N * 3 + T * N // 32))
+                self.ops.append(("quant", f"{g.name}.quant_X_128x1",
+                                 lambda X=X, st=st: st.update(b=fg.fp8_quant_act_1x128(X, rows=False, transposed=True)),
+                                 T * K * 3 + T * K // 32))
+                self.ops.append(("gemm", f"{g.name}.gemm",
+                                 lambda st=st, C=C: fg.fp8_gemm_blockscaled(st["a"][2], st["a"][3], st["b"][2],
+                                                                            st["b"][3], bkind=fg.BSCALE_ROW1x128,
+                                                                            out=C),
+                                 gemm_flops(g)))
+        self.gemm_flops = sum(w for k, _, _, w in self.ops if k == "gemm")
+
+    def step(self, events=None):
+        for i, (_, _, fn, _) in enumerate(self.ops):
+            if events is not None:
+                events[i][0].record()
+            fn()
+            if events is not None:
+                events[i][1].record()
+
+
+# -------------------------------------------------------------------- main --
+
+def run_device(args, rank, world, local_rank):
+    import torch
+    import fine_grained_fp8_weight_b300 as fg  # noqa: F401  (fails loudly if the library is missing)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    work = make_workload(args.workload)
+    path = DevicePath(work, dev)
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        path.step()
+    barrier()
+
+    n_ops = len(path.ops)
+    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n_ops)]
+              for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    barrier()
+    t0.record()
+    for s in range(args.steps):
+        path.step(events[s])
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    per_op = {}
+    for i, (kind, name, _, work_units) in enumerate(path.ops):
+        ms = [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(args.steps)]
+        avg = sum(ms) / len(ms)
+        entry = {"kind": kind, "ms": round(avg, 4)}
+        if kind == "gemm":
+            entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
+            entry["frac_fp8_peak"] = round(entry["TFLOP/s"] / fp8_peak, 4)
+        else:
+            entry["GB/s"] = round(work_units / (avg * 1e-3) / 1e9, 1)
+            entry["frac_hbm"] = round(entry["GB/s"] / peaks["hbm_gbs"], 4)
+        per_op[name] = entry
+
+    value = path.gemm_flops * world / (ms_step * 1e-3) / 1e12
+    gemm_ms = sum(e["ms"] for e in per_op.values() if e["kind"] == "gemm")
+    gemm_ach = path.gemm_flops / (gemm_ms * 1e-3) / 1e12
+    q_bytes = sum(w for k, _, _, w in path.ops if k == "quant")
+    q_ms = sum(e["ms"] for e in per_op.values() if e["kind"] == "quant")
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded numpy normals, bf16)",
+        "config": {"workload": work.name,
+                   "gemms": [n for k, n, _, _ in path.ops if k == "gemm"],
+                   "l2": "no flush: each step reads inputs larger than the 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_ach / fp8_peak, 4), "traffic": None,
+                     "kernel": "gemm_blockscaled_kernel",
+                     "peak_note": f"fp8 = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
+                                  f"{peaks['bf16_tflops']} TFLOP/s (sustained bf16 {peaks['bf16_tflops_sustained']})"},
+        "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "peak_hbm_gbs": peaks["hbm_gbs"],
+                     "frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "kernels": per_op,
+        "clocks": clk,
+        "gpu_launches": n_ops * args.steps,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(path, args, torch)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(work, args)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+def run_e2e(path, args, torch):
+    """Same metric through the public API from pinned host memory: every step
+    copies its BF16 inputs host->device, runs the path, and reads the outputs
+    back (device->host), all inside the timed region."""
+    from fine_grained_fp8_weight_b300 import workloads as wl
+    host_in = [wl.bf16_bits_to_torch(bits).pin_memory() for bits, _ in path.inputs]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in path.outputs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for h, (_, d) in zip(host_in, path.inputs):
+            d.copy_(h, non_blocking=True)
+        path.step()
+        for h, d in zip(host_out, path.outputs):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(steps):
+        e2e_step()
+    dt = (time.perf_counter() - t) / steps
+    return {"value": round(path.gemm_flops / dt / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def oracle_sample(work, rows, blocks):
+    """The oracle as it stands (single-threaded plain C) on a bounded sample of
+    each dense GEMM of the workload: `rows` activation rows quantized 1x128,
+    `blocks` 128-row blocks of the weight quantized 128x128, and the
+    rows x (128*blocks) block of the output in binary64.  Returns
+    (GEMM FLOPs of the sample, seconds)."""
+    import oracle
+    from fine_grained_fp8_weight_b300.workloads import Dense
+    flops = 0.0
+    t = time.perf_counter()
+    for g in work.gemms:
+        if not isinstance(g, Dense):
+            continue
+        N, K = g.B.shape
+        nb = min(blocks, (N + 127) // 128)
+        qa, sa = oracle.quant_act_1x128(np.ascontiguousarray(g.A[:rows]))
+        qb, sb = oracle.quant_w_128x128(np.ascontiguousarray(g.B[:nb * 128]))
+        oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
+        flops += 2.0 * qa.shape[0] * qb.shape[0] * K
+    return flops, time.perf_counter() - t
+
+
+def cpu_baseline(work, args):
+    flops, dt = oracle_sample(work, args.cpu_rows, args.cpu_blocks)
+    return {"value": round(flops / dt / 1e12, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"per GEMM: {args.cpu_rows} activation rows quantized 1x128, the first {args.cpu_blocks} "
+                      f"128-row weight blocks quantized 128x128, that {args.cpu_rows} x {128 * args.cpu_blocks} "
+                      f"output block in binary64 (single-threaded C oracle)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm is the oracle, run on the host cores on a bounded
+    sample of the same workload each step (8 rows x one 128-row weight block
+    per GEMM); rank 0 alone runs it."""
+    if rank != 0:
+        return None
+    work = make_workload(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample(work, 8, 1)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, dt = oracle_sample(work, 8, 1)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    return {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy normals, bf16)",
+            "config": {"workload": work.name, "parallelism": "host oracle, 1 thread"}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step and GEMM: 8 activation rows quantized 1x128, one 128-row weight "
+                                       "block quantized 128x128, the 8 x 128 output block in binary64"},
+            "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def profile_gemm(args):
+    """One warm-up and one timed launch of a single GEMM (for ncu captures)."""
+    import torch
+    import fine_grained_fp8_weight_b300 as fg
+    from fine_grained_fp8_weight_b300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    g = make_workload(args.workload).gemms[args.gemm_index]
+    A = wl.bf16_bits_to_torch(g.A).to(dev)
+    B = wl.bf16_bits_to_torch(g.B).to(dev)
+    qa, sa, _, _ = fg.fp8_quant_act_1x128(A)
+    qb, sb = fg.fp8_quant_w_128x128(B)
+    C = torch.empty((A.shape[0], B.shape[0]), dtype=torch.bfloat16, device=dev)
+    for _ in range(2):
+        fg.fp8_gemm_blockscaled(qa, sa, qb, sb, out=C)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    fg.fp8_gemm_blockscaled(qa, sa, qb, sb, out=C)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    print(json.dumps({"gemm": g.name, "ms": ms, "TFLOP/s": gemm_flops(g) / (ms * 1e-3) / 1e12}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "moe", "wgrad", "tiny"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--cpu-blocks", type=int, default=16)
+    ap.add_argument("--profile-gemm", action="store_true")
+    ap.add_argument("--gemm-index", type=int, default=0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3 and not args.profile_gemm:
+        print("note: fewer than 3 warm-up steps do not make a valid measurement", file=sys.stderr)
+    if args.profile_gemm:
+        profile_gemm(args)
+        return
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_device(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

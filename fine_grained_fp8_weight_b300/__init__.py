@@ -20,7 +20,8 @@ import os
 import torch
 
 __all__ = [
-    "FGF8Error", "lib", "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+    "FGF8Error", "lib", "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
+    "fp8_gemm_blockscaled",
     "fp8_grouped_gemm_blockscaled", "fgf8_mma_probe", "fgf8_read_status", "workspace_for",
     "BSCALE_BLOCK128", "BSCALE_ROW1x128", "OUT_BF16", "OUT_FP32",
 ]
@@ -39,6 +40,7 @@ STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED
 
 # Every symbol declared in include/fgf8.h and include/fgf8_testing.h.
 EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
+            "fp8_quant_w_128x128_grouped",
             "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled", "fgf8_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout"]
 
@@ -67,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.fgf8_version.restype = ctypes.c_char_p
         L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, P, I64, P, P, I64, P]
         L.fp8_quant_w_128x128.argtypes = [P, I64, I64, I64, P, P, I64, P]
+        L.fp8_quant_w_128x128_grouped.argtypes = [P, I32, I64, I64, I64, P, P, I64, P]
         L.fp8_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, ctypes.c_int, P, I64, ctypes.c_int,
                                            I64, I64, I64, P, SZ, P]
         L.fp8_grouped_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, P, I32, P, I64, ctypes.c_int,
@@ -76,7 +79,8 @@ def lib() -> ctypes.CDLL:
         L.fgf8_read_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
         L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
-        for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+        for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
+                     "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_blockscaled", "fgf8_read_status", "fgf8_mma_probe",
                      "fgf8_selftest_wait_timeout"):
             getattr(L, name).restype = ctypes.c_int
@@ -146,6 +150,18 @@ def fp8_quant_w_128x128(w: torch.Tensor):
     s = torch.empty((K // 128, round_up((N + 127) // 128, 4)), dtype=torch.float32, device=w.device)
     st = lib().fp8_quant_w_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), _ptr(s), s.shape[1], _stream(w.device))
     _check(st, "fp8_quant_w_128x128")
+    return q, s
+
+
+def fp8_quant_w_128x128_grouped(w: torch.Tensor):
+    """128x128 block quantization of stacked expert weights w: BF16 [E, N, K].
+    Returns (q [E, N, K], s [E, K/128, round_up(ceil(N/128), 4)])."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 3 and w.is_contiguous()
+    E, N, K = w.shape
+    q = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((E, K // 128, round_up((N + 127) // 128, 4)), dtype=torch.float32, device=w.device)
+    st = lib().fp8_quant_w_128x128_grouped(_ptr(w), E, N, K, K, _ptr(q), _ptr(s), s.shape[2], _stream(w.device))
+    _check(st, "fp8_quant_w_128x128_grouped")
     return q, s
 
 

@@ -109,7 +109,22 @@ fgf8_status fp8_quant_w_128x128(const void *w, int64_t N, int64_t K, int64_t ldw
     if (!aligned(w, 16) || ldw % 8 != 0 || !aligned(q, 16) || !aligned(s, 16)) return FGF8_ERR_MISALIGNED;
     fgf8_status st = current_device(nullptr);
     if (st != FGF8_OK) return st;
-    return from_cuda(fgf8::launch_quant_w(w, N, K, ldw, q, s, lds, static_cast<cudaStream_t>(stream)));
+    return from_cuda(fgf8::launch_quant_w(w, N, K, ldw, q, s, lds, 1, static_cast<cudaStream_t>(stream)));
+}
+
+fgf8_status fp8_quant_w_128x128_grouped(const void *w, int32_t num_experts, int64_t N, int64_t K, int64_t ldw,
+                                        uint8_t *q, float *s, int64_t lds, void *stream)
+{
+    if (num_experts < 0 || num_experts > 65535 || N < 0 || K <= 0) return FGF8_ERR_INVALID_ARG;
+    if (K % 128 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || num_experts == 0) return FGF8_OK;
+    if (w == nullptr || q == nullptr || s == nullptr || ldw < K) return FGF8_ERR_INVALID_ARG;
+    if (lds < (N + 127) / 128 || lds % 4 != 0) return FGF8_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || ldw % 8 != 0 || !aligned(q, 16) || !aligned(s, 16)) return FGF8_ERR_MISALIGNED;
+    fgf8_status st = current_device(nullptr);
+    if (st != FGF8_OK) return st;
+    return from_cuda(
+        fgf8::launch_quant_w(w, N, K, ldw, q, s, lds, num_experts, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts)

@@ -33,11 +33,14 @@ namespace {
 
 constexpr int BM = 128;                 // rows of A per tile (TMEM lanes)
 constexpr int BK = 128;                 // K elements (= bytes) per group
-constexpr int kThreads = 256;           // 8 warps
+constexpr int kThreads = 384;           // 12 warps: one control warpgroup, two promotion warpgroups
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kEpiWarp0 = 4;            // warps 4..7: TMEM lane quarters 0..3
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarp0 = 4;            // warps 4..11; warp w reads TMEM lane quarter w % 4
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kCtrlRegs = 56;      // registers per thread, control warpgroup
+constexpr uint32_t kEpiRegs = 224;      // registers per thread, promotion warpgroups
+static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= 384 * 168, "register split exceeds the launch budget");
 
 // wait-site ids reported in the status word
 enum : int32_t {
@@ -169,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_base_slot;
 
     const int32_t KB = p.KB;
+    if (warp < kEpiWarp0) regs_decrease<kCtrlRegs>();
 
     if (warp == kProducerWarp) {
         if (elect_one()) {
@@ -257,19 +261,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         mbar_wait(drain, 0, nullptr, 20u * 1000u * 1000u);
     } else if (warp >= kEpiWarp0) {
-        const uint32_t quarter = warp - kEpiWarp0;          // == warp % 4
+        regs_increase<kEpiRegs>();
+        constexpr int HALF = BN / 2;                        // columns per promotion warpgroup
+        constexpr int NCH = HALF / 32;                      // 32-column TMEM loads per K group
+        const uint32_t quarter = warp & 3;
+        const uint32_t half = (warp - kEpiWarp0) >> 2;      // 0: columns [0, HALF), 1: [HALF, BN)
         const uint32_t row = quarter * 32 + lane;
         const uint32_t lane_addr = (quarter * 32) << 16;
+        const uint32_t col0 = half * HALF;
         uint32_t it = 0;
         bool ok = true;
         for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
             int32_t mb, nb;
             tile_coords(tile, p, mb, nb);
             if (block_expert(p, mb) < 0) continue;
-            float acc[BN];
+            float acc[HALF];
 #pragma unroll
-            for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
-            const int sb_sel = ROW_SB ? 0 : ((nb * BN / 128) & 3);
+            for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+            const int sb_sel = ROW_SB ? 0 : ((nb * BN / 128) & 3) + (int)(col0 / 128);
             for (int32_t kb = 0; kb < KB; ++kb, ++it) {
                 const uint32_t j = it % SC, phj = (it / SC) & 1;
                 if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
@@ -278,6 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const float sa_v = sm_sa[j * BM + row];
+                const float *sbv = sm_sb + j * L::sb_slot + (ROW_SB ? col0 : 0);
+                const float blk_scale = ROW_SB ? 0.0f : sa_v * sm_sb[j * L::sb_slot + sb_sel];
                 const uint32_t buf = it & 1, phb = (it >> 1) & 1;
                 if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
                     record_timeout(p.status, kSiteEpiTmemFull);
@@ -285,21 +296,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const float *sbv = sm_sb + j * L::sb_slot;
+                const uint32_t taddr = tmem_base + lane_addr + buf * BN + col0;
+                uint32_t r[2][32];
+                tmem_ld_32x32b_x32(taddr, r[0]);
+                tmem_ld_wait(r[0]);
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + c * 32, r);
-                    tmem_ld_wait();
+                for (int c = 0; c < NCH; ++c) {
+                    if (c + 1 < NCH) tmem_ld_32x32b_x32(taddr + (c + 1) * 32, r[(c + 1) & 1]);
                     if (ROW_SB) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), sa_v * sbv[c * 32 + i], acc[c * 32 + i]);
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 sbq = *reinterpret_cast<const float4 *>(sbv + c * 32 + i);
+                            acc[c * 32 + i + 0] = fmaf(__uint_as_float(r[c & 1][i + 0]), sa_v * sbq.x, acc[c * 32 + i + 0]);
+                            acc[c * 32 + i + 1] = fmaf(__uint_as_float(r[c & 1][i + 1]), sa_v * sbq.y, acc[c * 32 + i + 1]);
+                            acc[c * 32 + i + 2] = fmaf(__uint_as_float(r[c & 1][i + 2]), sa_v * sbq.z, acc[c * 32 + i + 2]);
+                            acc[c * 32 + i + 3] = fmaf(__uint_as_float(r[c & 1][i + 3]), sa_v * sbq.w, acc[c * 32 + i + 3]);
+                        }
                     } else {
-                        const float scale = sa_v * sbv[sb_sel + (c * 32) / 128];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), scale, acc[c * 32 + i]);
+                        for (int i = 0; i < 32; ++i)
+                            acc[c * 32 + i] = fmaf(__uint_as_float(r[c & 1][i]), blk_scale, acc[c * 32 + i]);
                     }
+                    if (c + 1 < NCH) tmem_ld_wait(r[(c + 1) & 1]);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -309,22 +327,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            // write the finished row segment
+            // write this thread's finished row segment
             const int64_t m = (int64_t)mb * BM + row;
             bool write = m < p.M;
             if (write && p.m_indices) write = __ldg(p.m_indices + m) >= 0;
             if (write) {
-                const int64_t n0 = (int64_t)nb * BN;
+                const int64_t n0 = (int64_t)nb * BN + col0;
                 if (OUT_F32) {
                     float *dst = static_cast<float *>(p.C) + m * p.ldc + n0;
 #pragma unroll
-                    for (int c = 0; c < BN; c += 4)
+                    for (int c = 0; c < HALF; c += 4)
                         if (n0 + c < p.N)
                             *reinterpret_cast<float4 *>(dst + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
                 } else {
                     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.C) + m * p.ldc + n0;
 #pragma unroll
-                    for (int c = 0; c < BN; c += 8)
+                    for (int c = 0; c < HALF; c += 8)
                         if (n0 + c < p.N) store_row_bf16(dst + c, acc + c);
                 }
             }
@@ -345,8 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // in one TMEM accumulator (no promotion), raw FP32 written out.
 // ------------------------------------------------------------------------
 constexpr int kProbeMaxN = 256;
+constexpr int kProbeThreads = 256;      // warp 0 loads, warp 1 issues MMAs, warps 4..7 read TMEM
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kProbeThreads, 1)
     mma_probe_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float *D, int N,
                      int K, DeviceStatus *status)
 {
@@ -509,9 +528,11 @@ size_t gemm_workspace_bytes(int64_t, int64_t, int64_t, int32_t, int)
     return kWsHeaderBytes;
 }
 
-cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
+namespace {
+
+template <int BN>
+Params make_params(const GemmArgs &a)
 {
-    constexpr int BN = 128;
     Params p{};
     p.M = a.M;
     p.N = a.N;
@@ -527,14 +548,39 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
     p.b_rows_per_expert = a.m_indices ? a.N : 0;
     p.sb_rows_per_expert = a.m_indices ? p.KB : 0;
     p.status = reinterpret_cast<DeviceStatus *>(a.workspace);
+    return p;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    const Params p = make_params<BN>(a);
     const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
-    if (a.bkind == 1) {
-        return a.out_f32 ? launch_variant<BN, 6, 8, true, true>(a, p, grid, stream)
-                         : launch_variant<BN, 6, 8, true, false>(a, p, grid, stream);
-    }
-    return a.out_f32 ? launch_variant<BN, 6, 8, false, true>(a, p, grid, stream)
-                     : launch_variant<BN, 6, 8, false, false>(a, p, grid, stream);
+    if (a.bkind == 1)
+        return a.out_f32 ? launch_variant<BN, STAGES, 8, true, true>(a, p, grid, stream)
+                         : launch_variant<BN, STAGES, 8, true, false>(a, p, grid, stream);
+    return a.out_f32 ? launch_variant<BN, STAGES, 8, false, true>(a, p, grid, stream)
+                     : launch_variant<BN, STAGES, 8, false, false>(a, p, grid, stream);
+}
+
+// Tile width: 256 columns unless 128-column tiles fill the SMs' last wave
+// enough better to pay for their lower per-tile efficiency.
+int choose_bn(const GemmArgs &a, int num_sms)
+{
+    const int64_t mb = (a.M + BM - 1) / BM;
+    const int64_t t256 = mb * ((a.N + 255) / 256), t128 = mb * ((a.N + 127) / 128);
+    const double w256 = (double)((t256 + num_sms - 1) / num_sms) * 2.0;
+    const double w128 = (double)((t128 + num_sms - 1) / num_sms) * 1.15;
+    return w128 < w256 ? 128 : 256;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    if (choose_bn(a, num_sms) == 128) return launch_bn<128, 6>(a, stream, num_sms);
+    return launch_bn<256, 4>(a, stream, num_sms);
 }
 
 cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,
@@ -547,7 +593,7 @@ cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N
     const size_t smem = 1024 + BM * BK + kProbeMaxN * BK + 64;
     cudaError_t err = cudaFuncSetAttribute(mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    mma_probe_kernel<<<1, kThreads, smem, stream>>>(tmA, tmB, D, N, K, reinterpret_cast<DeviceStatus *>(workspace));
+    mma_probe_kernel<<<1, kProbeThreads, smem, stream>>>(tmA, tmB, D, N, K, reinterpret_cast<DeviceStatus *>(workspace));
     return cudaGetLastError();
 }
 

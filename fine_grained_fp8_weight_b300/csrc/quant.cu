@@ -205,6 +205,10 @@ __global__ void __launch_bounds__(kBlockThreads)
     __shared__ float red[kBlockThreads / 32];
     const int64_t kb = blockIdx.x;
     const int64_t nb = blockIdx.y;
+    // blockIdx.z: expert of a stacked [E][N][K] weight; its q and s follow it
+    w += (int64_t)blockIdx.z * N * ldw;
+    q += (int64_t)blockIdx.z * N * K;
+    s += (int64_t)blockIdx.z * (K / 128) * lds;
     const int64_t n0 = nb * 128;
     const int rows = (int)((N - n0) < 128 ? (N - n0) : 128);
     const int tid = threadIdx.x;
@@ -271,9 +275,9 @@ cudaError_t launch_quant_act_tiles(const void *x, int64_t M, int64_t K, int64_t 
 }
 
 cudaError_t launch_quant_w(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, float *s, int64_t lds,
-                           cudaStream_t stream)
+                           int32_t num_experts, cudaStream_t stream)
 {
-    const dim3 grid((unsigned)(K / 128), (unsigned)((N + 127) / 128));
+    const dim3 grid((unsigned)(K / 128), (unsigned)((N + 127) / 128), (unsigned)num_experts);
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     quant_w_block_kernel<<<grid, kBlockThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), N, K, ldw, q, s,
                                                              lds);

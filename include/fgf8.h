@@ -111,6 +111,20 @@ fgf8_status fp8_quant_w_128x128(const void *w, int64_t N, int64_t K, int64_t ldw
                                 uint8_t *q, float *s, int64_t lds, void *stream);
 
 /*
+ * fp8_quant_w_128x128_grouped -- the same 128x128 block quantization for a
+ * stack of expert weights (MoE), one launch for all experts, writing the
+ * per-expert scale layout that fp8_grouped_gemm_blockscaled reads.
+ *
+ *   w : BF16 [num_experts][N][ldw] (expert stride N*ldw), ldw >= K, ldw % 8 == 0.
+ *   q : E4M3 [num_experts][N][K].
+ *   s : float [num_experts][K/128][lds], s[(e*(K/128) + kb)*lds + nb];
+ *       lds >= ceil(N/128), lds % 4 == 0.
+ *   1 <= num_experts <= 65535 (0 is a no-op).  Alignment as above.
+ */
+fgf8_status fp8_quant_w_128x128_grouped(const void *w, int32_t num_experts, int64_t N, int64_t K,
+                                        int64_t ldw, uint8_t *q, float *s, int64_t lds, void *stream);
+
+/*
  * fp8_gemm_blockscaled -- C = A_hat * B_hat^T with per-group scales along the
  * inner dimension K ([dssusan] inner-dimension and E4M3 passages).  Each
  * 128-wide K partial product P = sum_{k in group} qa*qb is formed on the
