@@ -41,7 +41,8 @@ STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED
 # Every symbol declared in include/fgf8.h and include/fgf8_testing.h.
 EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
             "fp8_quant_w_128x128_grouped",
-            "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled", "fgf8_gemm_workspace_bytes",
+            "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm_blockscaled",
+            "fgf8_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout"]
 
 
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_w_128x128_grouped.argtypes = [P, I32, I64, I64, I64, P, P, I64, P]
         L.fp8_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, ctypes.c_int, P, I64, ctypes.c_int,
                                            I64, I64, I64, P, SZ, P]
+        L.fp8_gemm_blockscaled_noalloc.argtypes = [P, P, I64, P, P, I64, ctypes.c_int, P, I64, ctypes.c_int,
+                                                   I64, I64, I64, P]
         L.fp8_grouped_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, P, I32, P, I64, ctypes.c_int,
                                                    I64, I64, I64, P, SZ, P]
         L.fgf8_gemm_workspace_bytes.argtypes = [I64, I64, I64, I32]
@@ -80,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
         L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
         for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
-                     "fp8_gemm_blockscaled",
+                     "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc",
                      "fp8_grouped_gemm_blockscaled", "fgf8_read_status", "fgf8_mma_probe",
                      "fgf8_selftest_wait_timeout"):
             getattr(L, name).restype = ctypes.c_int

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "../../include/fgf8.h"
 #include "../../include/fgf8_testing.h"
@@ -187,6 +188,62 @@ fgf8_status fp8_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int6
     fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, 0, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M_total, N, K,
                      m_indices, num_experts, workspace, ws_bytes};
     return from_cuda(fgf8::launch_gemm(a, static_cast<cudaStream_t>(stream), num_sms));
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free GEMM entry point.  Its scratch (the device status word of the
+// GEMM kernel) lives in this file-scope device array instead of a workspace
+// the caller allocates.  Every device that loads the library holds the array
+// until the process exits; all calls on a device share it.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;        // 1 MiB per device
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mutex;
+void *g_static_scratch_ptr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the host-side name is only a stand-in, not a device address).
+fgf8_status static_scratch(void **ptr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FGF8_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FGF8_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return FGF8_ERR_CUDA;
+        g_static_scratch_ptr[dev] = p;
+    }
+    *ptr = g_static_scratch_ptr[dev];
+    return FGF8_OK;
+}
+
+}  // namespace
+
+fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int64_t ldsa, const uint8_t *B,
+                                         const float *sb, int64_t ldsb, fgf8_bscale_kind bkind, void *C,
+                                         int64_t ldc, fgf8_out_dtype cdt, int64_t M, int64_t N, int64_t K,
+                                         void *stream)
+{
+    if (M >= 1 && N >= 1 && K >= 1 && fgf8::gemm_workspace_bytes(M, N, K, 1, 0) > kStaticScratchBytes)
+        return FGF8_ERR_WORKSPACE_TOO_SMALL;
+    int num_sms = 0;
+    fgf8_status st = current_device(&num_sms);
+    if (st != FGF8_OK) return st;
+    void *ws = nullptr;
+    st = static_scratch(&ws);
+    if (st != FGF8_OK) return st;
+    st = check_gemm(A, sa, ldsa, B, sb, ldsb, bkind, C, ldc, cdt, M, N, K, ws, kStaticScratchBytes, 1);
+    if (st != FGF8_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the previous call's status word must not leak into this one
+    if (cudaMemsetAsync(ws, 0, fgf8::gemm_workspace_bytes(M, N, K, 1, 0), cs) != cudaSuccess) return FGF8_ERR_CUDA;
+    fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, (int)bkind, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M, N, K,
+                     nullptr, 1, ws, kStaticScratchBytes};
+    return from_cuda(fgf8::launch_gemm(a, cs, num_sms));
 }
 
 fgf8_status fgf8_read_status(void *workspace, void *stream, int32_t *site)

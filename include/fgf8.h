@@ -156,6 +156,38 @@ fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa
                                  void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * fp8_gemm_blockscaled_noalloc -- fp8_gemm_blockscaled for callers that may
+ * not allocate device memory: a plugin inside a host framework that owns all
+ * GPU memory and forbids allocations from plugins, or a latency-critical loop
+ * where an allocation could block or fragment the memory pool.  Such a caller
+ * cannot provide the workspace the other GEMM entry points need, so this one
+ * uses scratch inside the library instead.  The pages have no counterpart to
+ * this entry point; it exists for such callers only.
+ *
+ * Same arguments, layouts, checks and result as fp8_gemm_blockscaled, minus
+ * the workspace.  It allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine): its scratch is a 1 MiB array in device global
+ * memory that every device loading the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress) with the device current; make that first call
+ *     before any stream capture on the device.
+ *   - Shapes whose scratch need (fgf8_gemm_workspace_bytes(M, N, K, 1)) exceeds
+ *     1 MiB are rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; each call clears the part that must start at zero (the device
+ *     status word) on `stream` before its kernel.  Calls whose work can overlap
+ *     on the GPU (different streams, no ordering between them) race on the
+ *     array: order them, or use fp8_gemm_blockscaled with separate workspaces.
+ *   - A device-side wait that expires leaves its status in the shared array,
+ *     which no entry point reads back; the next call clears it.
+ */
+fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int64_t ldsa,
+                                         const uint8_t *B, const float *sb, int64_t ldsb,
+                                         fgf8_bscale_kind bkind,
+                                         void *C, int64_t ldc, fgf8_out_dtype cdt,
+                                         int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * fp8_grouped_gemm_blockscaled -- MoE expert GEMM in the contiguous layout:
  * the rows of A are grouped by expert, each group padded to a multiple of 128
  * rows, and row m uses expert e = m_indices[m] ([dssusan] scheme applied per
