@@ -43,7 +43,7 @@ EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_qu
             "fp8_quant_w_128x128_grouped",
             "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm_blockscaled",
             "fgf8_gemm_workspace_bytes",
-            "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout"]
+            "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div"]
 
 
 class FGF8Error(RuntimeError):
@@ -82,10 +82,11 @@ def lib() -> ctypes.CDLL:
         L.fgf8_read_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
         L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
+        L.fgf8_selftest_scaled_div.argtypes = [P, P, I64, P, P, P]
         for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
                      "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc",
                      "fp8_grouped_gemm_blockscaled", "fgf8_read_status", "fgf8_mma_probe",
-                     "fgf8_selftest_wait_timeout"):
+                     "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib

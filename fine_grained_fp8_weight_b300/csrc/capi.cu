@@ -89,6 +89,7 @@ fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx
     if (q != nullptr && (lds < M || lds % 4 != 0)) return FGF8_ERR_INVALID_ARG;
     if (qT != nullptr && (ldsT < K || ldsT % 4 != 0)) return FGF8_ERR_INVALID_ARG;
     if (qT != nullptr && M % 16 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (M * (K / 128) >= (int64_t(1) << 31)) return FGF8_ERR_UNSUPPORTED_SHAPE;   // 2^31 tiles
     if (!aligned(x, 16) || ldx % 8 != 0) return FGF8_ERR_MISALIGNED;
     if ((q && (!aligned(q, 16) || !aligned(s, 16))) || (qT && (!aligned(qT, 16) || !aligned(sT, 16))))
         return FGF8_ERR_MISALIGNED;
@@ -281,6 +282,15 @@ fgf8_status fgf8_selftest_wait_timeout(void *workspace, uint32_t budget_us, void
     fgf8_status st = current_device(nullptr);
     if (st != FGF8_OK) return st;
     return from_cuda(fgf8::launch_wait_timeout_selftest(workspace, budget_us, static_cast<cudaStream_t>(stream)));
+}
+
+fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, float *q_encoder,
+                                     float *q_ieee, void *stream)
+{
+    if (n < 0 || (n > 0 && (!x || !s || !q_encoder || !q_ieee))) return FGF8_ERR_INVALID_ARG;
+    fgf8_status st = current_device(nullptr);
+    if (st != FGF8_OK) return st;
+    return from_cuda(fgf8::launch_scaled_div_selftest(x, s, n, q_encoder, q_ieee, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

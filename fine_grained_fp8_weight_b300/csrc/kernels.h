@@ -12,6 +12,8 @@ cudaError_t launch_quant_act_rows(const void *x, int64_t M, int64_t K, int64_t l
                                   int64_t lds, cudaStream_t stream);
 cudaError_t launch_quant_act_tiles(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
                                    int64_t lds, uint8_t *qT, float *sT, int64_t ldsT, cudaStream_t stream);
+cudaError_t launch_scaled_div_selftest(const float *x, const float *s, int64_t n, float *fast, float *ieee,
+                                       cudaStream_t stream);
 cudaError_t launch_quant_w(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, float *s, int64_t lds,
                            int32_t num_experts, cudaStream_t stream);
 

@@ -12,6 +12,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace fgf8 {
 namespace {
@@ -27,11 +28,44 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
     return r;
 }
 
-// x / s with IEEE round-to-nearest; s == 0 only for an all-zero group, whose
-// elements are +-0 and encode to signed zeros directly.
-__device__ __forceinline__ float scaled(float x, float s)
+// Group divisor: s and its correctly rounded reciprocal.  `fast` is false for
+// s == 0 (all-zero group: the elements are +-0 and are encoded as they are),
+// for very small s and for s so large that 1/s would be subnormal; those
+// groups take the IEEE division.
+struct Divisor {
+    float s, r;
+    bool fast;
+};
+
+__device__ __forceinline__ Divisor make_divisor(float s)
 {
-    return s == 0.0f ? x : __fdiv_rn(x, s);
+    Divisor d;
+    d.s = s;
+    d.fast = s >= 0x1p-90f && s <= 0x1p125f;
+    d.r = d.fast ? __frcp_rn(s) : 0.0f;
+    return d;
+}
+
+// fl32(x / s) by Markstein's final-correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s) and
+// q0 = RN(x*r) within one ulp of x/s, the remainder e = x - s*q0 is exact in
+// one fused multiply-add and RN(q0 + e*r) is the correctly rounded quotient,
+// provided nothing overflows or underflows.  In a `fast` group (s >= 2^-90,
+// |x| <= 448 s) that holds for every |x| >= 2^-100; an element below that has
+// |x/s| < 2^-10, under the smallest E4M3 rounding midpoint, so it encodes to a
+// signed zero whichever binary32 neighbour the step returns.  The remainder is
+// formed negated, e' = s*q0 - x, and subtracted, q0 - e'*r: the same values
+// for x != 0, and for x = -0 the result keeps its sign (-0 - (+0) = -0).
+__device__ __forceinline__ float scaled(float x, const Divisor &d)
+{
+    if (d.fast) {
+        const float q0 = __fmul_rn(x, d.r);
+        const float en = __fmaf_rn(q0, d.s, -x);
+        return __fmaf_rn(-en, d.r, q0);
+    }
+    if (x == 0.0f || d.s == 0.0f) return x;     // +-0 / s keeps the sign of x; all-zero group
+    return __fdiv_rn(x, d.s);
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8])
@@ -44,7 +78,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8])
     }
 }
 
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s)
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], const Divisor &s)
 {
     uint2 o;
     o.x = cvt_e4m3x2(scaled(f[0], s), scaled(f[1], s)) | (cvt_e4m3x2(scaled(f[2], s), scaled(f[3], s)) << 16);
@@ -60,52 +94,66 @@ __device__ __forceinline__ float amax8(const float (&f)[8])
     return a;
 }
 
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------
-// 1x128 tiles along K.  A half-warp (16 lanes x 8 BF16) covers one tile; a
-// warp covers two consecutive tiles per round and kRounds rounds, with all
-// loads issued before any arithmetic so that enough bytes are in flight.
+// 1x128 tiles along K.  Eight lanes cover one tile (16 BF16 = 32 bytes each),
+// so a warp covers four consecutive tiles (1 KB) per load round; kActRounds
+// rounds are loaded before any arithmetic so that enough bytes are in flight.
 // ------------------------------------------------------------------------
-constexpr int kActRounds = 4;
+constexpr int kActRounds = 2;
 constexpr int kActWarps = 8;
 
 __global__ void __launch_bounds__(kActWarps * 32)
-    quant_act_rows_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t KB, int64_t ldx,
+    quant_act_rows_kernel(const __nv_bfloat16 *__restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
                           uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds)
 {
-    const int64_t total = M * KB;
+    const uint32_t total = M * KB;               // tiles; < 2^31, checked by the launcher
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;
-    const int sub = lane & 15;
-    const int64_t warp_global = (int64_t)blockIdx.x * kActWarps + (threadIdx.x >> 5);
-    const int64_t first = warp_global * (2 * kActRounds);
+    const int quad = lane >> 3;                  // which of the warp's four tiles
+    const int sub = lane & 7;                    // 16-element slice of the tile
+    const uint32_t warp_global = blockIdx.x * kActWarps + (threadIdx.x >> 5);
+    const int64_t K = (int64_t)KB * 128;
 
-    uint4 raw[kActRounds];
-    int64_t mrow[kActRounds], kblk[kActRounds];
+    uint4 raw[kActRounds][2];
+    uint32_t mrow[kActRounds], kblk[kActRounds];
 #pragma unroll
     for (int r = 0; r < kActRounds; ++r) {
-        const int64_t t = first + 2 * r + half;
-        mrow[r] = -1;
-        raw[r] = make_uint4(0, 0, 0, 0);
+        const uint32_t t = (warp_global * kActRounds + r) * 4 + quad;
+        raw[r][0] = raw[r][1] = make_uint4(0, 0, 0, 0);
+        mrow[r] = 0xFFFFFFFFu;
         if (t < total) {
-            mrow[r] = t / KB;
-            kblk[r] = t - mrow[r] * KB;
-            const __nv_bfloat16 *src = x + mrow[r] * ldx + kblk[r] * 128 + sub * 8;
-            raw[r] = __ldcs(reinterpret_cast<const uint4 *>(src));
+            const uint32_t m = t / KB;
+            mrow[r] = m;
+            kblk[r] = t - m * KB;
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)m * ldx + (int64_t)kblk[r] * 128 + sub * 16);
+            raw[r][0] = __ldcs(src);
+            raw[r][1] = __ldcs(src + 1);
         }
     }
 #pragma unroll
     for (int r = 0; r < kActRounds; ++r) {
-        float f[8];
-        bf16x8_to_f32(raw[r], f);
-        float a = amax8(f);
+        float f[2][8];
+        bf16x8_to_f32(raw[r][0], f[0]);
+        bf16x8_to_f32(raw[r][1], f[1]);
+        float a = fmaxf(amax8(f[0]), amax8(f[1]));
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (mrow[r] >= 0) {
+        for (int o = 4; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (mrow[r] != 0xFFFFFFFFu) {
             const float sc = __fdiv_rn(a, kE4M3Max);
-            const uint2 codes = encode8(f, sc);
-            const int64_t K = KB * 128;
-            *reinterpret_cast<uint2 *>(q + mrow[r] * K + kblk[r] * 128 + sub * 8) = codes;
-            if (sub == 0) s[kblk[r] * lds + mrow[r]] = sc;
+            const Divisor dv = make_divisor(sc);
+            const uint2 lo = encode8(f[0], dv), hi = encode8(f[1], dv);
+            *reinterpret_cast<uint4 *>(q + (int64_t)mrow[r] * K + (int64_t)kblk[r] * 128 + sub * 16) =
+                make_uint4(lo.x, lo.y, hi.x, hi.y);
+            if (sub == 0) s[(int64_t)kblk[r] * lds + mrow[r]] = sc;
         }
     }
 }
@@ -154,6 +202,7 @@ __global__ void __launch_bounds__(kTileThreads)
         __syncthreads();
         const float amax = fmaxf(part[0][ch], part[1][ch]);
         const float sc = __fdiv_rn(amax, kE4M3Max);
+        const Divisor dv = make_divisor(sc);
         if (h == 0) sT[tb * ldsT + kb * 128 + ch] = sc;
         // encode this thread's 64 tokens of channel ch into qT[kb*128+ch][m0 + h*64 ...]
         uint8_t *dst = qT + (kb * 128 + ch) * M + m0 + h * 64;
@@ -168,7 +217,7 @@ __global__ void __launch_bounds__(kTileThreads)
                 float f1 = __bfloat162float(tile[(r0 + 4 * j + 1) * kTilePitch + ch]);
                 float f2 = __bfloat162float(tile[(r0 + 4 * j + 2) * kTilePitch + ch]);
                 float f3 = __bfloat162float(tile[(r0 + 4 * j + 3) * kTilePitch + ch]);
-                w[j] = cvt_e4m3x2(scaled(f0, sc), scaled(f1, sc)) | (cvt_e4m3x2(scaled(f2, sc), scaled(f3, sc)) << 16);
+                w[j] = cvt_e4m3x2(scaled(f0, dv), scaled(f1, dv)) | (cvt_e4m3x2(scaled(f2, dv), scaled(f3, dv)) << 16);
             }
             *reinterpret_cast<uint4 *>(dst + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -186,22 +235,26 @@ __global__ void __launch_bounds__(kTileThreads)
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
             const float sc = __fdiv_rn(a, kE4M3Max);
-            *reinterpret_cast<uint2 *>(q + (m0 + r) * K + kb * 128 + sub * 8) = encode8(f, sc);
+            *reinterpret_cast<uint2 *>(q + (m0 + r) * K + kb * 128 + sub * 8) = encode8(f, make_divisor(sc));
             if (sub == 0) s[kb * lds + m0 + r] = sc;
         }
     }
 }
 
 // ------------------------------------------------------------------------
-// 128x128 weight blocks: one CTA per block, the block held in registers
-// (8 x 16 bytes per thread) across the max-abs reduction and the encode.
+// 128x128 weight blocks: one CTA per block.  The block (32 KB of BF16) is
+// staged in shared memory with asynchronous 16-byte copies, so that registers
+// do not limit how many blocks an SM keeps in flight; each thread then reads
+// back the chunks it copied for the max-abs and again for the encode.
 // ------------------------------------------------------------------------
 constexpr int kBlockThreads = 256;
+constexpr int kBlockChunks = 128 * 16 / kBlockThreads;     // 16-byte chunks per thread
 
 __global__ void __launch_bounds__(kBlockThreads)
     quant_w_block_kernel(const __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
                          uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds)
 {
+    __shared__ __align__(16) uint4 tile[128 * 16];
     __shared__ float red[kBlockThreads / 32];
     const int64_t kb = blockIdx.x;
     const int64_t nb = blockIdx.y;
@@ -213,19 +266,19 @@ __global__ void __launch_bounds__(kBlockThreads)
     const int rows = (int)((N - n0) < 128 ? (N - n0) : 128);
     const int tid = threadIdx.x;
 
-    uint4 raw[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kBlockChunks; ++i) {
         const int c = tid + i * kBlockThreads;
         const int r = c >> 4, c16 = c & 15;
-        raw[i] = make_uint4(0, 0, 0, 0);
-        if (r < rows) raw[i] = __ldcs(reinterpret_cast<const uint4 *>(w + (n0 + r) * ldw + kb * 128 + c16 * 8));
+        if (r < rows) cp_async_16(&tile[c], w + (n0 + r) * ldw + kb * 128 + c16 * 8);
+        else tile[c] = make_uint4(0, 0, 0, 0);
     }
+    cp_async_wait_all();
     float a = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kBlockChunks; ++i) {
         float f[8];
-        bf16x8_to_f32(raw[i], f);
+        bf16x8_to_f32(tile[tid + i * kBlockThreads], f);
         a = fmaxf(a, amax8(f));
     }
 #pragma unroll
@@ -236,31 +289,51 @@ __global__ void __launch_bounds__(kBlockThreads)
 #pragma unroll
     for (int i = 1; i < kBlockThreads / 32; ++i) amax = fmaxf(amax, red[i]);
     const float sc = __fdiv_rn(amax, kE4M3Max);
+    const Divisor dv = make_divisor(sc);
     if (tid == 0) s[kb * lds + nb] = sc;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kBlockChunks; ++i) {
         const int c = tid + i * kBlockThreads;
         const int r = c >> 4, c16 = c & 15;
         if (r < rows) {
             float f[8];
-            bf16x8_to_f32(raw[i], f);
-            *reinterpret_cast<uint2 *>(q + (n0 + r) * K + kb * 128 + c16 * 8) = encode8(f, sc);
+            bf16x8_to_f32(tile[c], f);
+            *reinterpret_cast<uint2 *>(q + (n0 + r) * K + kb * 128 + c16 * 8) = encode8(f, dv);
         }
     }
 }
 
+// Test hook: the quotient the encoders use next to CUDA's IEEE division.
+__global__ void scaled_div_selftest_kernel(const float *__restrict__ x, const float *__restrict__ s, int64_t n,
+                                           float *__restrict__ fast, float *__restrict__ ieee)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        fast[i] = scaled(x[i], make_divisor(s[i]));
+        ieee[i] = __fdiv_rn(x[i], s[i]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_scaled_div_selftest(const float *x, const float *s, int64_t n, float *fast, float *ieee,
+                                       cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    scaled_div_selftest_kernel<<<1184, 256, 0, stream>>>(x, s, n, fast, ieee);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act_rows(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
                                   int64_t lds, cudaStream_t stream)
 {
     const int64_t KB = K / 128;
     const int64_t tiles = M * KB;
-    const int64_t per_block = (int64_t)kActWarps * 2 * kActRounds;
+    if (tiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // 2^31 tiles = 2^38 elements
+    const int64_t per_block = (int64_t)kActWarps * kActRounds * 4;
     const int64_t blocks = (tiles + per_block - 1) / per_block;
     if (blocks == 0) return cudaSuccess;
     quant_act_rows_kernel<<<(unsigned)blocks, kActWarps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(x), M, KB, ldx, q, s, lds);
+        static_cast<const __nv_bfloat16 *>(x), (uint32_t)M, (uint32_t)KB, ldx, q, s, lds);
     return cudaGetLastError();
 }
 

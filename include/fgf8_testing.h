@@ -26,6 +26,16 @@ extern "C" {
  */
 fgf8_status fgf8_selftest_wait_timeout(void *workspace, uint32_t budget_us, void *stream);
 
+/*
+ * fgf8_selftest_scaled_div -- for i < n, q_encoder[i] = the binary32 quotient
+ * x[i] / s[i] exactly as the quantization kernels compute it (a correctly
+ * rounded reciprocal of s and one fused correction step), and q_ieee[i] =
+ * CUDA's IEEE round-to-nearest division, so that a test can check that the
+ * two agree bit for bit.  Device pointers, float32, n >= 0.
+ */
+fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, float *q_encoder,
+                                     float *q_ieee, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
