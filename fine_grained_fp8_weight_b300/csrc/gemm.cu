@@ -36,10 +36,13 @@ constexpr int BK = 128;                 // K elements (= bytes) per group
 constexpr int kThreads = 384;           // 12 warps: one control warpgroup, two promotion warpgroups
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kEpiWarp0 = 4;            // warps 4..11; warp w reads TMEM lane quarter w % 4
+constexpr int kScaleWarp = 2;
+constexpr int kEpiWarp0 = 4;            // warps 4..11; warp w may read TMEM lanes 32*(w%4) .. +31
 constexpr int kEpiWarps = 8;
-constexpr uint32_t kCtrlRegs = 56;      // registers per thread, control warpgroup
-constexpr uint32_t kEpiRegs = 224;      // registers per thread, promotion warpgroups
+// Registers per thread after the split (the launch gives 168 to every thread):
+// the control warpgroup gives some back, the promotion warpgroups take them.
+constexpr uint32_t kCtrlRegs = 40;
+constexpr uint32_t kEpiRegs = 232;
 static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= 384 * 168, "register split exceeds the launch budget");
 
 // wait-site ids reported in the status word
@@ -107,13 +110,13 @@ __device__ __forceinline__ int32_t block_expert(const Params &p, int32_t mb)
     return p.m_indices ? __ldg(p.m_indices + (int64_t)mb * BM) : 0;
 }
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float *v)
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, float2 a, float2 b, float2 c, float2 d)
 {
     uint4 o;
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
-    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+    __nv_bfloat162 h0 = __float22bfloat162_rn(a);
+    __nv_bfloat162 h1 = __float22bfloat162_rn(b);
+    __nv_bfloat162 h2 = __float22bfloat162_rn(c);
+    __nv_bfloat162 h3 = __float22bfloat162_rn(d);
     memcpy(&o.x, &h0, 4);
     memcpy(&o.y, &h1, 4);
     memcpy(&o.z, &h2, 4);
@@ -188,8 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t e = block_expert(p, mb);
                 if (e < 0) continue;
                 const int32_t b_row = (int32_t)(e * p.b_rows_per_expert) + nb * BN;
-                const int32_t s_row0 = e * p.sb_rows_per_expert;
-                const int32_t sb_x = ROW_SB ? nb * BN : ((nb * BN / 128) & ~3);
                 for (int32_t kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
@@ -200,6 +201,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(L::a_bytes + L::b_bytes));
                     tma_load_2d(sm_a + s * L::a_bytes, &tmA, &full[s], kb * BK, mb * BM);
                     tma_load_2d(sm_b + s * L::b_bytes, &tmB, &full[s], kb * BK, b_row);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                // let the copies already issued land before the CTA exits
+                const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0;
+                for (uint32_t i = first; i <= it; ++i)
+                    mbar_wait(&full[i % STAGES], (i / STAGES) & 1, nullptr, 20u * 1000u * 1000u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kScaleWarp) {
+        // The scale vectors of each K group (512 bytes of sa, and 16 bytes of
+        // block sb or BN*4 bytes of per-row sb) stream through their own ring,
+        // so they run up to SC groups ahead, independent of the A/B stages.
+        if (elect_one()) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+                int32_t mb, nb;
+                tile_coords(tile, p, mb, nb);
+                const int32_t e = block_expert(p, mb);
+                if (e < 0) continue;
+                const int32_t s_row0 = e * p.sb_rows_per_expert;
+                const int32_t sb_x = ROW_SB ? nb * BN : ((nb * BN / 128) & ~3);
+                for (int32_t kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t j = it % SC, phj = (it / SC) & 1;
                     if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
                         record_timeout(p.status, kSiteProducerScale);
@@ -213,10 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 *abort_flag = 1;
-                // let the copies already issued land before the CTA exits
-                const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0;
+                const uint32_t first = it > (uint32_t)SC ? it - SC : 0;
                 for (uint32_t i = first; i <= it; ++i)
-                    mbar_wait(&full[i % STAGES], (i / STAGES) & 1, nullptr, 20u * 1000u * 1000u);
+                    mbar_wait(&sc_full[i % SC], (i / SC) & 1, nullptr, 20u * 1000u * 1000u);
             }
         }
         __syncwarp();
@@ -262,10 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, 0, nullptr, 20u * 1000u * 1000u);
     } else if (warp >= kEpiWarp0) {
         regs_increase<kEpiRegs>();
-        constexpr int HALF = BN / 2;                        // columns per promotion warpgroup
+        // Promotion warpgroups: warps 4..7 cover TMEM lane quarters 0..3 for the
+        // first half of the tile's columns, warps 8..11 for the second half.
+        constexpr int HALF = BN / 2;                        // columns per promotion warp
         constexpr int NCH = HALF / 32;                      // 32-column TMEM loads per K group
         const uint32_t quarter = warp & 3;
-        const uint32_t half = (warp - kEpiWarp0) >> 2;      // 0: columns [0, HALF), 1: [HALF, BN)
+        const uint32_t half = (warp - kEpiWarp0) >> 2;
         const uint32_t row = quarter * 32 + lane;
         const uint32_t lane_addr = (quarter * 32) << 16;
         const uint32_t col0 = half * HALF;
@@ -275,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t mb, nb;
             tile_coords(tile, p, mb, nb);
             if (block_expert(p, mb) < 0) continue;
-            float acc[HALF];
+            float2 acc[HALF / 2];
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < HALF / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
             const int sb_sel = ROW_SB ? 0 : ((nb * BN / 128) & 3) + (int)(col0 / 128);
             for (int32_t kb = 0; kb < KB; ++kb, ++it) {
                 const uint32_t j = it % SC, phj = (it / SC) & 1;
@@ -288,7 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float sa_v = sm_sa[j * BM + row];
                 const float *sbv = sm_sb + j * L::sb_slot + (ROW_SB ? col0 : 0);
-                const float blk_scale = ROW_SB ? 0.0f : sa_v * sm_sb[j * L::sb_slot + sb_sel];
+                const float blk = ROW_SB ? 0.0f : sa_v * sm_sb[j * L::sb_slot + sb_sel];
+                const float2 blk2 = make_float2(blk, blk);
+                const float2 sa2 = make_float2(sa_v, sa_v);
                 const uint32_t buf = it & 1, phb = (it >> 1) & 1;
                 if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
                     record_timeout(p.status, kSiteEpiTmemFull);
@@ -297,27 +327,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + lane_addr + buf * BN + col0;
-                uint32_t r[2][32];
-                tmem_ld_32x32b_x32(taddr, r[0]);
-                tmem_ld_wait(r[0]);
+                // 64 columns per round: two loads in flight, one wait, then the FMAs
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    if (c + 1 < NCH) tmem_ld_32x32b_x32(taddr + (c + 1) * 32, r[(c + 1) & 1]);
-                    if (ROW_SB) {
+                for (int g = 0; g < NCH / 2; ++g) {
+                    uint32_t r[2][32];
+                    tmem_ld_32x32b_x32(taddr + (2 * g) * 32, r[0]);
+                    tmem_ld_32x32b_x32(taddr + (2 * g + 1) * 32, r[1]);
+                    tmem_ld_wait(r[0]);
+                    reg_fence(r[1]);
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 sbq = *reinterpret_cast<const float4 *>(sbv + c * 32 + i);
-                            acc[c * 32 + i + 0] = fmaf(__uint_as_float(r[c & 1][i + 0]), sa_v * sbq.x, acc[c * 32 + i + 0]);
-                            acc[c * 32 + i + 1] = fmaf(__uint_as_float(r[c & 1][i + 1]), sa_v * sbq.y, acc[c * 32 + i + 1]);
-                            acc[c * 32 + i + 2] = fmaf(__uint_as_float(r[c & 1][i + 2]), sa_v * sbq.z, acc[c * 32 + i + 2]);
-                            acc[c * 32 + i + 3] = fmaf(__uint_as_float(r[c & 1][i + 3]), sa_v * sbq.w, acc[c * 32 + i + 3]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 2 * g + h;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 pv = make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1]));
+                            if (ROW_SB) {
+                                const float2 sbp = *reinterpret_cast<const float2 *>(sbv + c * 32 + 2 * i);
+                                acc[c * 16 + i] = __ffma2_rn(pv, __fmul2_rn(sa2, sbp), acc[c * 16 + i]);
+                            } else {
+                                acc[c * 16 + i] = __ffma2_rn(pv, blk2, acc[c * 16 + i]);
+                            }
                         }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + i] = fmaf(__uint_as_float(r[c & 1][i]), blk_scale, acc[c * 32 + i]);
                     }
-                    if (c + 1 < NCH) tmem_ld_wait(r[(c + 1) & 1]);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -338,12 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < HALF; c += 4)
                         if (n0 + c < p.N)
-                            *reinterpret_cast<float4 *>(dst + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                            *reinterpret_cast<float4 *>(dst + c) =
+                                make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
                 } else {
                     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.C) + m * p.ldc + n0;
 #pragma unroll
                     for (int c = 0; c < HALF; c += 8)
-                        if (n0 + c < p.N) store_row_bf16(dst + c, acc + c);
+                        if (n0 + c < p.N) store_bf16x8(dst + c, acc[c / 2], acc[c / 2 + 1], acc[c / 2 + 2], acc[c / 2 + 3]);
                 }
             }
         }
@@ -558,10 +590,10 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
     const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
     if (a.bkind == 1)
-        return a.out_f32 ? launch_variant<BN, STAGES, 8, true, true>(a, p, grid, stream)
-                         : launch_variant<BN, STAGES, 8, true, false>(a, p, grid, stream);
-    return a.out_f32 ? launch_variant<BN, STAGES, 8, false, true>(a, p, grid, stream)
-                     : launch_variant<BN, STAGES, 8, false, false>(a, p, grid, stream);
+        return a.out_f32 ? launch_variant<BN, STAGES, 12, true, true>(a, p, grid, stream)
+                         : launch_variant<BN, STAGES, 12, true, false>(a, p, grid, stream);
+    return a.out_f32 ? launch_variant<BN, STAGES, 12, false, true>(a, p, grid, stream)
+                     : launch_variant<BN, STAGES, 12, false, false>(a, p, grid, stream);
 }
 
 // Tile width: 256 columns unless 128-column tiles fill the SMs' last wave
