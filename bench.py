@@ -9,7 +9,9 @@ One step = the whole path over the prefill projection pair (GEMM1 4096 x
 ``value`` is the step's GEMM FLOPs (2*M*N*K summed over both GEMMs) divided by
 the device time of the step, with all inputs resident in HBM (BF16 inputs of
 738 MB per step, larger than the 126 MB L2, so no flush is needed between
-steps).  The JSON line also carries the roofline of the dominant kernel (the
+steps).  The step is captured once as a CUDA graph and replayed, so that the
+timed region holds device work only; per-kernel times replay each op's own
+graph with an L2 flush between replays.  The JSON line also carries the roofline of the dominant kernel (the
 GEMM), per-kernel times, quantize bandwidth, an end-to-end figure through the
 public API with pinned host buffers, and the CPU oracle timed on a bounded
 sample.
@@ -35,6 +37,16 @@ import numpy as np  # noqa: E402
 
 METRIC = "block-scaled FP8 GEMM TFLOP/s (% of FP8 peak); quantize GB/s (% of HBM)"
 FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
+
+# DRAM bytes (read + write) of one launch, from an ncu capture of that exact
+# kernel build (profiles/ holds the summaries).  Keyed by the library version
+# string, which changes whenever a kernel changes, so a stale figure is never
+# reported: a kernel without a capture of its current build reports null.
+MEASURED_TRAFFIC = {
+    "fgf8 0.2 sm_103a": {
+        "prefill_pair_4096x18432x7168/up.gemm": 295773440,   # profiles/gemm_blockscaled_prefill_up.md
+    },
+}
 
 
 def load_peaks():
@@ -242,17 +254,29 @@ def run_device(args, rank, world, local_rank):
         path.step()
     barrier()
 
-    n_ops = len(path.ops)
-    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n_ops)]
-              for _ in range(args.steps)]
+    # The step is captured once into a CUDA graph and replayed, so that host
+    # launch overhead does not enter the device-timed region.
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        path.step()                                  # allocations settle outside the capture
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(step_graph, stream=stream):
+            path.step()
+    torch.cuda.current_stream(dev).wait_stream(stream)
+    for _ in range(args.warmup):
+        step_graph.replay()
+    barrier()
+
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     clocks.start()
     barrier()
     t0.record()
-    for s in range(args.steps):
-        path.step(events[s])
+    for _ in range(args.steps):
+        step_graph.replay()
     t1.record()
     barrier()
     clk = clocks.stop()
@@ -262,10 +286,30 @@ def run_device(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
+
+    # Per-kernel device time: each op captured alone and replayed, one event
+    # pair per replay, with an untimed write of a buffer larger than L2 in
+    # between so that no op reads inputs left in L2 by its previous replay.
+    flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
     per_op = {}
-    for i, (kind, name, _, work_units) in enumerate(path.ops):
-        ms = [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(args.steps)]
-        avg = sum(ms) / len(ms)
+    reps = max(3, min(args.op_reps, args.steps))
+    for kind, name, fn, work_units in path.ops:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        torch.cuda.current_stream(dev).wait_stream(stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        g.replay()
+        for e0, e1 in ev:
+            flush.fill_(1.0)
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize(dev)
+        avg = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps
         entry = {"kind": kind, "ms": round(avg, 4)}
         if kind == "gemm":
             entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
@@ -274,10 +318,15 @@ def run_device(args, rank, world, local_rank):
             entry["GB/s"] = round(work_units / (avg * 1e-3) / 1e9, 1)
             entry["frac_hbm"] = round(entry["GB/s"] / peaks["hbm_gbs"], 4)
         per_op[name] = entry
+    n_ops = len(path.ops)
 
     value = path.gemm_flops * world / (ms_step * 1e-3) / 1e12
-    gemm_ms = sum(e["ms"] for e in per_op.values() if e["kind"] == "gemm")
-    gemm_ach = path.gemm_flops / (gemm_ms * 1e-3) / 1e12
+    # roofline of the dominant kernel: the GEMM launch that takes longest
+    gemm_ops = [(per_op[name]["ms"], name, w) for kind, name, _, w in path.ops if kind == "gemm"]
+    dom_ms, dom_name, dom_flops = max(gemm_ops)
+    gemm_ach = dom_flops / (dom_ms * 1e-3) / 1e12
+    version = fg.lib().fgf8_version().decode()
+    traffic = MEASURED_TRAFFIC.get(version, {}).get(f"{work.name}/{dom_name}")
     q_bytes = sum(w for k, _, _, w in path.ops if k == "quant")
     q_ms = sum(e["ms"] for e in per_op.values() if e["kind"] == "quant")
     result = {
@@ -290,8 +339,9 @@ def run_device(args, rank, world, local_rank):
                    "l2": "no flush: each step reads inputs larger than the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_ach / fp8_peak, 4), "traffic": None,
-                     "kernel": "gemm_blockscaled_kernel",
+                     "unit": "TFLOP/s", "frac": round(gemm_ach / fp8_peak, 4), "traffic": traffic,
+                     "kernel": f"gemm_blockscaled_kernel ({dom_name}, {version})",
+                     "algorithmic_flops_per_launch": dom_flops,
                      "peak_note": f"fp8 = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
                                   f"{peaks['bf16_tflops']} TFLOP/s (sustained bf16 {peaks['bf16_tflops_sustained']})"},
         "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "peak_hbm_gbs": peaks["hbm_gbs"],
@@ -421,7 +471,7 @@ def profile_gemm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "moe", "wgrad", "tiny"])
@@ -429,6 +479,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--cpu-blocks", type=int, default=16)
+    ap.add_argument("--op-reps", type=int, default=20)
     ap.add_argument("--profile-gemm", action="store_true")
     ap.add_argument("--gemm-index", type=int, default=0)
     args = ap.parse_args()
