@@ -57,7 +57,21 @@ def test_dense_shapes(M, N, K, out):
     assert_within_bound(Cg, Cr, S, f"{M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 256, 512), (256, 144, 384)])
+# Larger M: several M blocks per N block, a ragged last M block, odd and even
+# K-group counts, and N past the last tile column.
+@pytest.mark.parametrize("M,N,K", [(256, 128, 128), (257, 144, 384), (600, 400, 512), (1024, 16, 256),
+                                   (768, 256, 640)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_dense_large_m(M, N, K, out):
+    rng = np.random.default_rng(M * 13 + N * 5 + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (N, K), 0.02)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    Cg, Cr, S = _run_dense(A, B, dt)
+    assert_within_bound(Cg, Cr, S, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 256, 512), (256, 144, 384), (512, 256, 1024)])
 def test_row_scaled_b(M, N, K):
     rng = np.random.default_rng(M + N + K)
     A = wl.bf16_normal(rng, (M, K), 1.0, 0.001, 50.0)
