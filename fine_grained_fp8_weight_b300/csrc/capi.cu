@@ -73,7 +73,7 @@ const char *fgf8_status_string(fgf8_status st)
 
 const char *fgf8_version(void)
 {
-    return "fgf8 0.2 sm_103a";
+    return "fgf8 0.3 sm_103a";
 }
 
 fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
@@ -240,8 +240,8 @@ fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int6
     st = check_gemm(A, sa, ldsa, B, sb, ldsb, bkind, C, ldc, cdt, M, N, K, ws, kStaticScratchBytes, 1);
     if (st != FGF8_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // the previous call's status word must not leak into this one
-    if (cudaMemsetAsync(ws, 0, fgf8::gemm_workspace_bytes(M, N, K, 1, 0), cs) != cudaSuccess) return FGF8_ERR_CUDA;
+    // the previous call's status word (and split-K counters) must not leak into this one
+    if (cudaMemsetAsync(ws, 0, fgf8::gemm_workspace_zeroed_bytes(M, N, K, 1), cs) != cudaSuccess) return FGF8_ERR_CUDA;
     fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, (int)bkind, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M, N, K,
                      nullptr, 1, ws, kStaticScratchBytes};
     return from_cuda(fgf8::launch_gemm(a, cs, num_sms));

@@ -327,29 +327,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + lane_addr + buf * BN + col0;
-                // 64 columns per round: two loads in flight, one wait, then the FMAs
+                if constexpr (ROW_SB) {
+                    // per-column B scales: twice the FP work per element, so one
+                    // 32-column load at a time (keeps the register budget spill-free)
 #pragma unroll
-                for (int g = 0; g < NCH / 2; ++g) {
-                    uint32_t r[2][32];
-                    tmem_ld_32x32b_x32(taddr + (2 * g) * 32, r[0]);
-                    tmem_ld_32x32b_x32(taddr + (2 * g + 1) * 32, r[1]);
-                    tmem_ld_wait(r[0]);
-                    reg_fence(r[1]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = 2 * g + h;
+                    for (int c = 0; c < NCH; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_sync<32>(taddr + c * 32, r);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float2 pv = make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1]));
-                            if (ROW_SB) {
-                                const float2 sbp = *reinterpret_cast<const float2 *>(sbv + c * 32 + 2 * i);
-                                acc[c * 16 + i] = __ffma2_rn(pv, __fmul2_rn(sa2, sbp), acc[c * 16 + i]);
-                            } else {
-                                acc[c * 16 + i] = __ffma2_rn(pv, blk2, acc[c * 16 + i]);
-                            }
+                            const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                            const float2 sbp = *reinterpret_cast<const float2 *>(sbv + c * 32 + 2 * i);
+                            acc[c * 16 + i] = __ffma2_rn(pv, __fmul2_rn(sa2, sbp), acc[c * 16 + i]);
+                        }
+                    }
+                } else {
+                    // 64 columns per load and wait, then the FMAs
+#pragma unroll
+                    for (int g = 0; g < NCH / 2; ++g) {
+                        uint32_t r[64];
+                        tmem_ld_sync<64>(taddr + g * 64, r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                            acc[g * 32 + i] = __ffma2_rn(pv, blk2, acc[g * 32 + i]);
                         }
                     }
                 }
+                fence_proxy_async_smem();     // scale slot j is refilled by TMA once released
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -380,6 +385,322 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) *abort_flag = 1;
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, L::tmem_cols);
+    }
+}
+
+
+// ------------------------------------------------------------------------
+// Small M (decode, M <= 256 tokens): the weight tile fills the MMA's M = 128
+// side and the tokens its N side (NT = M rounded up to 16), i.e. D^T = W X^T
+// per 128 weight rows, so the MMA shape suits a handful of tokens.  Such GEMMs
+// read 128 x K bytes of weights per 2*128*NT*K FLOP, far below the tensor
+// cores' ridge ("kailasan.com recruit post 147436", decode passage: the batch
+// per expert is small and memory access is the bottleneck), so the K groups
+// are split across CTAs until every SM streams weights.  Each split's FP32
+// partial goes to the workspace; the last CTA of a weight tile to take an
+// atomic ticket adds the partials in split order (deterministic), writes the
+// output and resets the ticket.  No CTA waits for another.
+// Promotion: acc[token] += P[w_row][token] * (sb[w block][kb] * sa[kb][token]).
+// ------------------------------------------------------------------------
+constexpr int kMaxSplits = 8;   // split-K factor of the small-M kernel, at most
+
+struct SmallParams {
+    int64_t M, N, K;
+    int32_t KB, S, n_tiles;
+    void *C;
+    int64_t ldc;
+    float *partials;          // [n_tiles][S][NT][128]
+    uint32_t *tickets;        // [n_tiles], zero between calls
+    DeviceStatus *status;
+};
+
+template <int NT, int STAGES, int SC>
+struct SmallLayout {
+    static constexpr size_t w_bytes = (size_t)BM * BK;        // 16 KB of weights
+    static constexpr size_t x_bytes = (size_t)NT * BK;        // tokens
+    static constexpr size_t off_w = 0;
+    static constexpr size_t off_x = off_w + STAGES * w_bytes;
+    static constexpr int sa_slot = NT < 32 ? 32 : NT;          // floats; 128-byte aligned TMA targets
+    static constexpr size_t off_sa = align_up(off_x + STAGES * x_bytes, 1024);
+    static constexpr size_t off_sb = off_sa + (size_t)SC * sa_slot * 4;
+    static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * 32 * 4, 16);
+    // as many TMEM partial buffers as fit (up to 8): the MMA can run ahead of
+    // the promotion by that many K groups
+    static constexpr int nbuf = (512 / NT) < 8 ? (512 / NT) : 8;
+    static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1;
+    static constexpr size_t off_misc = off_bar + (size_t)num_bars * 8;
+    static constexpr size_t total = off_misc + 16;
+    static constexpr size_t dyn_bytes = total + 1024;
+    static constexpr uint32_t tmem_cols = nbuf * NT < 32 ? 32 : nbuf * NT;   // power of two
+};
+
+template <int NT, int STAGES, int SC, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_smallm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                       const SmallParams p)
+{
+    using L = SmallLayout<NT, STAGES, SC>;
+    constexpr int COLS = NT / 2;                 // token columns per promotion warp
+    constexpr int CH = COLS < 32 ? COLS : 32;    // columns per TMEM load
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
+    uint8_t *sm_w = smem + L::off_w;
+    uint8_t *sm_x = smem + L::off_x;
+    float *sm_sa = reinterpret_cast<float *>(smem + L::off_sa);
+    float *sm_sb = reinterpret_cast<float *>(smem + L::off_sb);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *sc_full = bars + 2 * STAGES;
+    uint64_t *sc_empty = bars + 2 * STAGES + SC;
+    uint64_t *tm_full = bars + 2 * STAGES + 2 * SC;
+    uint64_t *tm_empty = tm_full + L::nbuf;
+    uint64_t *drain = tm_full + 2 * L::nbuf;
+    uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + L::off_misc + 4);   // [0] abort, [1] last
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+    const int32_t tile = blockIdx.x / p.S;       // 128 weight rows
+    const int32_t split = blockIdx.x - tile * p.S;
+    const int32_t kb0 = (int32_t)((int64_t)split * p.KB / p.S);
+    const int32_t kb1 = (int32_t)((int64_t)(split + 1) * p.KB / p.S);
+    const int32_t ngroups = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < SC; ++i) {
+            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < L::nbuf; ++i) {
+            mbar_init(&tm_full[i], 1);
+            mbar_init(&tm_empty[i], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_base_slot, L::tmem_cols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_base_slot;
+    volatile int *abort_flag = flags;
+    // register split: the promotion warpgroups' increase below draws on what
+    // the control warpgroup gives back here (128*40 + 256*232 <= 384*168)
+    if (warp < kEpiWarp0) regs_decrease<kCtrlRegs>();
+
+    if (warp == kProducerWarp) {
+        if (elect_one()) {
+            tma_prefetch_desc(&tmW);
+            tma_prefetch_desc(&tmX);
+            for (int32_t g = 0; g < ngroups; ++g) {
+                const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                    record_timeout(p.status, kSiteProducerEmpty);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + L::x_bytes));
+                tma_load_2d(sm_w + s * L::w_bytes, &tmW, &full[s], (kb0 + g) * BK, tile * BM);
+                tma_load_2d(sm_x + s * L::x_bytes, &tmX, &full[s], (kb0 + g) * BK, 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kScaleWarp) {
+        if (elect_one()) {
+            tma_prefetch_desc(&tmSA);
+            tma_prefetch_desc(&tmSB);
+            for (int32_t g = 0; g < ngroups; ++g) {
+                const uint32_t j = g % SC, phj = (g / SC) & 1;
+                if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+                    record_timeout(p.status, kSiteProducerScale);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(NT * 4 + 16));
+                tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], 0, kb0 + g);
+                tma_load_2d(sm_sb + j * 32, &tmSB, &sc_full[j], tile & ~3, kb0 + g);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        const uint32_t idesc = idesc_e4m3_f32(BM, NT);
+        bool ok = true;
+        for (int32_t g = 0; g < ngroups; ++g) {
+            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+            const uint32_t buf = g % L::nbuf, phb = (g / L::nbuf) & 1;
+            if (!mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
+                record_timeout(p.status, kSiteMmaTmemEmpty);
+                ok = false;
+                break;
+            }
+            if (!mbar_wait(&full[s], ph, abort_flag)) {
+                record_timeout(p.status, kSiteMmaFull);
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            if (elect_one()) {
+                const uint64_t dw = smem_desc_kmajor_sw128(sm_w + s * L::w_bytes);
+                const uint64_t dx = smem_desc_kmajor_sw128(sm_x + s * L::x_bytes);
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k)
+                    mma_e4m3(tmem_base + buf * NT, dw + 2 * k, dx + 2 * k, idesc, k > 0 ? 1u : 0u);
+                mma_commit(&empty[s]);
+                mma_commit(&tm_full[buf]);
+            }
+            __syncwarp();
+        }
+        if (!ok) *abort_flag = 1;
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait(drain, 0, nullptr, 20u * 1000u * 1000u);
+    } else if (warp >= kEpiWarp0) {
+        regs_increase<kEpiRegs>();
+        const uint32_t quarter = warp & 3;
+        const uint32_t half = (warp - kEpiWarp0) >> 2;
+        const uint32_t wrow = quarter * 32 + lane;              // weight row in the tile
+        const uint32_t lane_addr = (quarter * 32) << 16;
+        const uint32_t col0 = half * COLS;                      // first token column
+        float2 acc[COLS / 2];
+#pragma unroll
+        for (int i = 0; i < COLS / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        bool ok = true;
+        for (int32_t g = 0; g < ngroups; ++g) {
+            const uint32_t j = g % SC, phj = (g / SC) & 1;
+            if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
+                record_timeout(p.status, kSiteEpiScale);
+                ok = false;
+                break;
+            }
+            const float sbw = sm_sb[j * 32 + (tile & 3)];
+            const float2 sbw2 = make_float2(sbw, sbw);
+            const float *sav = sm_sa + j * L::sa_slot + col0;
+            const uint32_t buf = g % L::nbuf, phb = (g / L::nbuf) & 1;
+            if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
+                record_timeout(p.status, kSiteEpiTmemFull);
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < COLS; c += CH) {
+                uint32_t r[CH];
+                tmem_ld_sync<CH>(tmem_base + lane_addr + buf * NT + col0 + c, r);
+#pragma unroll
+                for (int i = 0; i < CH / 2; ++i) {
+                    const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    const float2 sa2 = *reinterpret_cast<const float2 *>(sav + c + 2 * i);
+                    acc[c / 2 + i] = __ffma2_rn(pv, __fmul2_rn(sbw2, sa2), acc[c / 2 + i]);
+                }
+            }
+            fence_proxy_async_smem();         // scale slot j is refilled by TMA once released
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&tm_empty[buf]);
+                mbar_arrive(&sc_empty[j]);
+            }
+        }
+        if (!ok) *abort_flag = 1;
+        const int64_t n = (int64_t)tile * BM + wrow;
+        if (ok && p.S == 1) {
+            if (n < p.N) {
+#pragma unroll
+                for (int i = 0; i < COLS / 2; ++i) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t m = col0 + 2 * i + h;
+                        const float v = h ? acc[i].y : acc[i].x;
+                        if (m < p.M) {
+                            if (OUT_F32) static_cast<float *>(p.C)[m * p.ldc + n] = v;
+                            else static_cast<__nv_bfloat16 *>(p.C)[m * p.ldc + n] = __float2bfloat16_rn(v);
+                        }
+                    }
+                }
+            }
+        } else if (p.S > 1) {
+            // this split's partial: [column][weight row], one 128-byte row per warp store
+            float *part = p.partials + ((int64_t)tile * p.S + split) * NT * BM;
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < COLS / 2; ++i) {
+                    part[(int64_t)(col0 + 2 * i) * BM + wrow] = acc[i].x;
+                    part[(int64_t)(col0 + 2 * i + 1) * BM + wrow] = acc[i].y;
+                }
+            }
+            __threadfence();
+            // all eight promotion warps have written; none gave up?
+            const bool all_ok = named_barrier_and(1, kEpiWarps * 32, ok && !*abort_flag);
+            if (all_ok && threadIdx.x == kEpiWarp0 * 32) {
+                const uint32_t ticket = atomicAdd(p.tickets + tile, 1u);
+                const int last = ticket == (uint32_t)p.S - 1;
+                if (last) p.tickets[tile] = 0u;                 // ready for the next call
+                flags[1] = last;
+            }
+            named_barrier_sync(1, kEpiWarps * 32);
+            if (all_ok && flags[1]) {
+                // last split of this weight tile: add the partials in split
+                // order, four outputs per float4, kRedUnroll of them in flight
+                __threadfence();
+                constexpr int kRedUnroll = 4;
+                constexpr int E4 = NT * BM / 4;                 // float4 per partial
+                const float4 *base = reinterpret_cast<const float4 *>(p.partials + (int64_t)tile * p.S * NT * BM);
+                const int t = (int)threadIdx.x - kEpiWarp0 * 32;   // 0 .. 255
+                for (int e0 = t; e0 < E4; e0 += kEpiWarps * 32 * kRedUnroll) {
+                    float4 v[kRedUnroll][kMaxSplits];
+#pragma unroll
+                    for (int u = 0; u < kRedUnroll; ++u) {
+                        const int e = e0 + u * kEpiWarps * 32;
+#pragma unroll
+                        for (int sidx = 0; sidx < kMaxSplits; ++sidx)
+                            if (sidx < p.S && e < E4) v[u][sidx] = __ldcg(base + (int64_t)sidx * E4 + e);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kRedUnroll; ++u) {
+                        const int e = e0 + u * kEpiWarps * 32;
+                        if (e >= E4) continue;
+                        float4 sum = v[u][0];
+#pragma unroll
+                        for (int sidx = 1; sidx < kMaxSplits; ++sidx) {
+                            if (sidx < p.S) {
+                                sum.x += v[u][sidx].x;
+                                sum.y += v[u][sidx].y;
+                                sum.z += v[u][sidx].z;
+                                sum.w += v[u][sidx].w;
+                            }
+                        }
+                        const int col = (e * 4) / BM, r = e * 4 - col * BM;
+                        const int64_t n = (int64_t)tile * BM + r;
+                        if (col >= p.M || n >= p.N) continue;      // N % 16 == 0: all four in or out
+                        if (OUT_F32) {
+                            *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + (int64_t)col * p.ldc + n) = sum;
+                        } else {
+                            const __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x, sum.y);
+                            const __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z, sum.w);
+                            uint2 o;
+                            memcpy(&o.x, &lo, 4);
+                            memcpy(&o.y, &hi, 4);
+                            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.C) + (int64_t)col * p.ldc + n) = o;
+                        }
+                    }
+                }
+            }
+        }
     }
 
     tc_fence_before_sync();
@@ -460,8 +781,7 @@ __global__ void __launch_bounds__(kProbeThreads, 1)
         const uint32_t row = quarter * 32 + lane;
         for (int c = 0; c < N; c += 32) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + ((quarter * 32) << 16) + c, r);
-            tmem_ld_wait();
+            tmem_ld_sync<32>(tmem + ((quarter * 32) << 16) + c, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 if (c + i < N) D[(int64_t)row * N + c + i] = __uint_as_float(r[i]);
@@ -555,9 +875,55 @@ bool make_tensor_map_2d(void *map, int dtype_bytes, bool is_float, const void *b
     return r == CUDA_SUCCESS;
 }
 
-size_t gemm_workspace_bytes(int64_t, int64_t, int64_t, int32_t, int)
+namespace {
+
+// Token columns of the small-M kernel: M rounded up to 16, 32, 64, 128 or 256.
+int small_nt(int64_t M)
 {
-    return kWsHeaderBytes;
+    return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+}
+
+bool use_small_m(int64_t M, int64_t N, int32_t num_experts_or_dense, int num_sms)
+{
+    (void)num_experts_or_dense;
+    return M <= 256 && (N + BM - 1) / BM <= (num_sms > 0 ? num_sms / 2 : 74);
+}
+
+int small_splits(int64_t N, int64_t K, int num_sms)
+{
+    const int64_t tiles = (N + BM - 1) / BM, KB = K / BK;
+    int64_t S = (num_sms > 0 ? num_sms : 148) / tiles;
+    if (S > kMaxSplits) S = kMaxSplits;
+    if (S > KB) S = KB;
+    return S < 1 ? 1 : (int)S;
+}
+
+size_t round256(size_t v)
+{
+    return (v + 255) / 256 * 256;
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int)
+{
+    size_t bytes = kWsHeaderBytes;
+    if (num_experts <= 1 && M <= 256) {
+        // small-M split-K: arrival tickets and FP32 partials, sized for the
+        // largest split count any device could choose
+        const int64_t tiles = (N + BM - 1) / BM;
+        const int64_t smax = K / BK < kMaxSplits ? K / BK : kMaxSplits;
+        bytes += round256((size_t)tiles * 4);
+        bytes += (size_t)tiles * smax * small_nt(M) * BM * 4;
+    }
+    return bytes;
+}
+
+size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t, int32_t num_experts)
+{
+    size_t bytes = kWsHeaderBytes;
+    if (num_experts <= 1 && M <= 256) bytes += round256((size_t)((N + BM - 1) / BM) * 4);
+    return bytes;
 }
 
 namespace {
@@ -596,6 +962,48 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
                      : launch_variant<BN, STAGES, 12, false, false>(a, p, grid, stream);
 }
 
+template <int NT, int STAGES, bool OUT_F32>
+cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    using L = SmallLayout<NT, STAGES, 8>;
+    SmallParams p{};
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.KB = (int32_t)(a.K / BK);
+    p.n_tiles = (int32_t)((a.N + BM - 1) / BM);
+    p.S = small_splits(a.N, a.K, num_sms);
+    p.C = a.C;
+    p.ldc = a.ldc;
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    p.status = reinterpret_cast<DeviceStatus *>(ws);
+    p.tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
+    p.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + round256((size_t)p.n_tiles * 4));
+    CUtensorMap tmW, tmX, tmSA, tmSB;
+    if (!make_tensor_map_2d(&tmW, 1, false, a.B, a.K, a.N, a.K, BK, BM, true) ||
+        !make_tensor_map_2d(&tmX, 1, false, a.A, a.K, a.M, a.K, BK, NT, true) ||
+        !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, 1, false) ||
+        !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, p.KB, a.ldsb * 4, 4, 1, false))
+        return cudaErrorInvalidValue;
+    auto kern = gemm_smallm_kernel<NT, STAGES, 8, OUT_F32>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
+    if (err != cudaSuccess) return err;
+    kern<<<p.n_tiles * p.S, kThreads, L::dyn_bytes, stream>>>(tmW, tmX, tmSA, tmSB, p);
+    return cudaGetLastError();
+}
+
+template <bool OUT_F32>
+cudaError_t launch_small_nt(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    switch (small_nt(a.M)) {
+    case 16: return launch_small<16, 8, OUT_F32>(a, stream, num_sms);
+    case 32: return launch_small<32, 8, OUT_F32>(a, stream, num_sms);
+    case 64: return launch_small<64, 8, OUT_F32>(a, stream, num_sms);
+    case 128: return launch_small<128, 6, OUT_F32>(a, stream, num_sms);
+    default: return launch_small<256, 4, OUT_F32>(a, stream, num_sms);
+    }
+}
+
 // Tile width: 256 columns unless 128-column tiles fill the SMs' last wave
 // enough better to pay for their lower per-tile efficiency.
 int choose_bn(const GemmArgs &a, int num_sms)
@@ -611,6 +1019,9 @@ int choose_bn(const GemmArgs &a, int num_sms)
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
+    // Few tokens: weights on the MMA's M side, K split across the SMs.
+    if (a.m_indices == nullptr && a.bkind == 0 && use_small_m(a.M, a.N, 1, num_sms))
+        return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
     if (choose_bn(a, num_sms) == 128) return launch_bn<128, 6>(a, stream, num_sms);
     return launch_bn<256, 4>(a, stream, num_sms);
 }

@@ -35,10 +35,14 @@ struct GemmArgs {
     size_t ws_bytes;
 };
 
-// Workspace layout: [0, 256) status word; split-K partials and counters after.
+// Workspace layout: [0, 256) status word; then, for small M, the split-K
+// arrival counters (one per 128 weight rows) and the FP32 partial sums.
 constexpr size_t kWsHeaderBytes = 256;
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int num_sms);
+// Leading part of the workspace that must be zero when a call starts (the
+// status word and the split-K arrival counters).
+size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
 cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,
                              cudaStream_t stream);

@@ -78,6 +78,13 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8])
     }
 }
 
+// Channel j (0..7) of 8 packed BF16 values, as binary32.
+__device__ __forceinline__ float bf16_lane(const uint4 &v, int j)
+{
+    const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
 __device__ __forceinline__ uint2 encode8(const float (&f)[8], const Divisor &s)
 {
     uint2 o;
@@ -159,84 +166,82 @@ __global__ void __launch_bounds__(kActWarps * 32)
 }
 
 // ------------------------------------------------------------------------
-// 128 tokens x 128 channels per CTA, staged in shared memory: the column
-// (token-direction, 128x1) groups give the transposed output qT/sT; when q/s
-// are requested too, the row (1x128) groups of the same tile are encoded
-// from the same staged data.  M % 16 == 0 when qT is written.
+// 128 tokens x 128 channels per CTA, held in registers: thread t owns the 8
+// channels of 16-byte column chunk c = t % 16 for the 8 consecutive tokens
+// 8g .. 8g+7, g = t / 16.  Column (token-direction, 128x1) max-abs: over the
+// thread's 8 tokens, across the two half-warps (one shuffle) and across the
+// eight warps (shared memory).  Row (1x128) max-abs, when q/s are wanted too:
+// over the thread's 8 channels and across its half-warp (four shuffles).  The
+// transposed output qT[channel][token] is written as 8-byte token runs.
+// M % 16 == 0 when qT is written, so a thread's 8 tokens are all present or
+// all absent.
 // ------------------------------------------------------------------------
 constexpr int kTileThreads = 256;
-constexpr int kTilePitch = 128 + 8;   // BF16 elements per staged row (pad breaks bank conflicts)
 
 __global__ void __launch_bounds__(kTileThreads)
     quant_act_tile_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
                           uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds,
                           uint8_t *__restrict__ qT, float *__restrict__ sT, int64_t ldsT)
 {
-    __shared__ __align__(16) __nv_bfloat16 tile[128 * kTilePitch];
-    __shared__ float part[2][128];
-
+    __shared__ float colmax[kTileThreads / 32][128];
     const int64_t kb = blockIdx.x;          // channel group
     const int64_t tb = blockIdx.y;          // token group
     const int64_t m0 = tb * 128;
-    const int rows = (int)((M - m0) < 128 ? (M - m0) : 128);
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c16 = tid & 15;               // channels 8*c16 .. 8*c16+7 of the group
+    const int g = tid >> 4;                 // tokens 8*g .. 8*g+7 of the group
+    const int64_t tok0 = m0 + 8 * g;
+    const bool present = tok0 < M;          // all 8 or none (M % 16 == 0)
 
-    // stage: 128 rows x 256 bytes = 2048 chunks of 16 bytes, 8 per thread
+    uint4 raw[8];                           // [token]: 8 packed BF16 channels
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int c = tid + i * kTileThreads;
-        const int r = c >> 4, c16 = c & 15;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < rows) v = __ldcs(reinterpret_cast<const uint4 *>(x + (m0 + r) * ldx + kb * 128 + c16 * 8));
-        *reinterpret_cast<uint4 *>(&tile[r * kTilePitch + c16 * 8]) = v;
+        raw[i] = make_uint4(0, 0, 0, 0);
+        if (present) raw[i] = __ldcs(reinterpret_cast<const uint4 *>(x + (tok0 + i) * ldx + kb * 128 + c16 * 8));
+    }
+
+    // --- column groups (128x1): the transposed output
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(bf16_lane(raw[i], j)));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        if (lane < 16) colmax[warp][c16 * 8 + j] = a;
     }
     __syncthreads();
-
     if (qT != nullptr) {
-        // two threads per channel, 64 tokens each
-        const int ch = tid & 127;
-        const int h = tid >> 7;
-        float a = 0.0f;
-        for (int r = h * 64; r < h * 64 + 64; ++r) a = fmaxf(a, fabsf(__bfloat162float(tile[r * kTilePitch + ch])));
-        part[h][ch] = a;
-        __syncthreads();
-        const float amax = fmaxf(part[0][ch], part[1][ch]);
-        const float sc = __fdiv_rn(amax, kE4M3Max);
-        const Divisor dv = make_divisor(sc);
-        if (h == 0) sT[tb * ldsT + kb * 128 + ch] = sc;
-        // encode this thread's 64 tokens of channel ch into qT[kb*128+ch][m0 + h*64 ...]
-        uint8_t *dst = qT + (kb * 128 + ch) * M + m0 + h * 64;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int r0 = h * 64 + g * 16;
-            if (r0 >= rows) break;          // rows is a multiple of 16 here
-            uint32_t w[4];
+        for (int j = 0; j < 8; ++j) {
+            float a = colmax[0][c16 * 8 + j];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float f0 = __bfloat162float(tile[(r0 + 4 * j + 0) * kTilePitch + ch]);
-                float f1 = __bfloat162float(tile[(r0 + 4 * j + 1) * kTilePitch + ch]);
-                float f2 = __bfloat162float(tile[(r0 + 4 * j + 2) * kTilePitch + ch]);
-                float f3 = __bfloat162float(tile[(r0 + 4 * j + 3) * kTilePitch + ch]);
-                w[j] = cvt_e4m3x2(scaled(f0, dv), scaled(f1, dv)) | (cvt_e4m3x2(scaled(f2, dv), scaled(f3, dv)) << 16);
+            for (int w = 1; w < kTileThreads / 32; ++w) a = fmaxf(a, colmax[w][c16 * 8 + j]);
+            const float sc = __fdiv_rn(a, kE4M3Max);
+            if (g == 0) sT[tb * ldsT + kb * 128 + c16 * 8 + j] = sc;
+            if (present) {
+                float col[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) col[i] = bf16_lane(raw[i], j);
+                *reinterpret_cast<uint2 *>(qT + (kb * 128 + c16 * 8 + j) * M + tok0) = encode8(col, make_divisor(sc));
             }
-            *reinterpret_cast<uint4 *>(dst + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 
+    // --- row groups (1x128), from the same registers
     if (q != nullptr) {
-        // row groups: 16 lanes per token row, 8 channels per lane
-        const int lane = tid & 31, sub = lane & 15;
-        const int row_in_pass = (tid >> 4);          // 0..15
-        for (int r = row_in_pass; r < rows; r += kTileThreads / 16) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r * kTilePitch + sub * 8]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             float f[8];
-            bf16x8_to_f32(v, f);
+            bf16x8_to_f32(raw[i], f);
             float a = amax8(f);
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            const float sc = __fdiv_rn(a, kE4M3Max);
-            *reinterpret_cast<uint2 *>(q + (m0 + r) * K + kb * 128 + sub * 8) = encode8(f, make_divisor(sc));
-            if (sub == 0) s[kb * lds + m0 + r] = sc;
+            if (present) {
+                const float sc = __fdiv_rn(a, kE4M3Max);
+                *reinterpret_cast<uint2 *>(q + (tok0 + i) * K + kb * 128 + c16 * 8) = encode8(f, make_divisor(sc));
+                if (c16 == 0) s[kb * lds + tok0 + i] = sc;
+            }
         }
     }
 }

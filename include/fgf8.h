@@ -175,7 +175,8 @@ fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa
  *     1 MiB are rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any launch.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; each call clears the part that must start at zero (the device
- *     status word) on `stream` before its kernel.  Calls whose work can overlap
+ *     status word and, for M <= 256, the split-K arrival counters) on `stream`
+ *     before its kernel.  Calls whose work can overlap
  *     on the GPU (different streams, no ordering between them) race on the
  *     array: order them, or use fp8_gemm_blockscaled with separate workspaces.
  *   - A device-side wait that expires leaves its status in the shared array,

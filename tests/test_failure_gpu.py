@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 def test_timeout_is_reported_and_context_survives():
     L = ensure_built()
-    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(max(4096, L.fgf8_gemm_workspace_bytes(128, 256, 512, 1)), dtype=torch.uint8, device=DEV)
     st = L.fgf8_selftest_wait_timeout(fg._ptr(ws), 20000, fg._stream(ws.device))
     assert st == 0
     status, site = fg.fgf8_read_status(ws)

@@ -23,6 +23,10 @@ def _d(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
+def _sample_rows(M, n, seed):
+    return np.sort(np.random.default_rng(seed).choice(M, size=min(n, M), replace=False))
+
+
 def _run_dense(Abits, Bbits, out_dtype, rows=None, bkind=0):
     qa, sa = oracle.quant_act_1x128(Abits)
     if bkind == 0:
@@ -69,6 +73,41 @@ def test_dense_large_m(M, N, K, out):
     dt = torch.bfloat16 if out == "bf16" else torch.float32
     Cg, Cr, S = _run_dense(A, B, dt)
     assert_within_bound(Cg, Cr, S, f"{M}x{N}x{K}")
+
+
+# M <= 256 takes the small-M path (weights on the MMA's M side, K split over
+# the SMs, last-arriving split adds the partials): every token width 16..256,
+# a ragged last weight tile, 1 to 8 splits, both output types.
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 7168), (5, 144, 2048), (33, 512, 1024), (64, 7168, 2048),
+                                   (100, 400, 640), (200, 1024, 3072), (256, 2048, 512), (250, 16, 128)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_small_m(M, N, K, out):
+    rng = np.random.default_rng(M * 17 + N + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (N, K), 0.02)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    rows = _sample_rows(M, 40, M) if M * N * K > 2 ** 31 else None
+    Cg, Cr, S = _run_dense(A, B, dt, rows=rows)
+    assert_within_bound(Cg, Cr, S, f"small {M}x{N}x{K}")
+
+
+def test_small_m_repeated_calls_same_workspace():
+    # the split-K arrival counters must be back at zero after every call
+    rng = np.random.default_rng(77)
+    A = wl.bf16_normal(rng, (48, 1024))
+    B = wl.bf16_normal(rng, (1024, 1024), 0.02)
+    qa, sa = oracle.quant_act_1x128(A)
+    qb, sb = oracle.quant_w_128x128(B)
+    ws = torch.zeros(fg.lib().fgf8_gemm_workspace_bytes(48, 1024, 1024, 1) + 4096, dtype=torch.uint8, device=DEV)
+    outs = [fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb)
+    for o in outs:
+        assert_within_bound(bf16_out_to_f64(o), Cr, S)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2]), "split order must be deterministic"
+    assert fg.fgf8_read_status(ws) == (0, 0)
+    tickets = ws[256:256 + 8 * 4].view(torch.int32)
+    assert int(tickets.abs().sum()) == 0
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 256, 512), (256, 144, 384), (512, 256, 1024)])
@@ -140,9 +179,6 @@ def test_grouped_small(counts):
 
 # --- full-size workloads, sampled rows ---
 
-def _sample_rows(M, n, seed):
-    return np.sort(np.random.default_rng(seed).choice(M, size=min(n, M), replace=False))
-
 
 def test_full_size_prefill_pair_sampled():
     for g, seed in zip(wl.prefill_pair().gemms, (11, 12)):
@@ -168,3 +204,35 @@ def test_full_size_wgrad_sampled():
     rows = _sample_rows(dYt.shape[0], 3, 14)
     Cr, S = oracle.gemm_blockscaled(dYt, sdY, Xt, sX, 1, rows=rows)
     assert_within_bound(C.cpu().numpy().astype(np.float64)[rows], Cr, S, "wgrad")
+
+
+# Every path adds in a fixed order (small-M adds its K splits in split order
+# too): repeated launches on the same operands must agree bit for bit over the
+# whole output.  A race between the tensor-memory loads, the scale ring and its
+# TMA refills, or the output stores shows up here as a differing element long
+# before a sampled comparison with the oracle sees it.  The shapes give every
+# CTA several tiles (the scale ring then runs into the next tile), on both
+# tile widths, both B-scale kinds and both output types, plus small M.
+@pytest.mark.parametrize("M,N,K,bkind,out", [(2048, 4096, 4096, 0, "bf16"), (4096, 2048, 4096, 1, "fp32"),
+                                             (4096, 2048, 4096, 1, "bf16"), (4096, 4096, 2048, 0, "fp32"),
+                                             (3072, 1792, 2048, 1, "fp32"), (3072, 1792, 2048, 0, "bf16"),
+                                             (64, 7168, 4096, 0, "bf16"), (200, 2048, 4096, 0, "fp32")])
+def test_repeated_launches_bitwise_identical(M, N, K, bkind, out):
+    g = torch.Generator(device="cpu").manual_seed(M + N + K + bkind)
+    qa = torch.randint(0, 256, (M, K), dtype=torch.uint8, generator=g)
+    qa[(qa & 0x7F) == 0x7F] = 0x3C                  # no NaN codes
+    qb = torch.randint(0, 256, (N, K), dtype=torch.uint8, generator=g)
+    qb[(qb & 0x7F) == 0x7F] = 0x3C
+    sa = torch.rand((K // 128, M), generator=g) + 0.5
+    if bkind == 0:
+        sb = torch.rand((K // 128, ((N + 127) // 128 + 3) // 4 * 4), generator=g) + 0.5   # row stride % 4 == 0
+    else:
+        sb = torch.rand((K // 128, N), generator=g) + 0.5
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    args = [t.to(DEV) for t in (qa, sa, qb, sb)]
+    outs = [fg.fp8_gemm_blockscaled(*args, bkind=bkind, out_dtype=dt) for _ in range(6)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs[1:], 1):
+        bad = (o.view(torch.int16 if dt == torch.bfloat16 else torch.int32)
+               != outs[0].view(torch.int16 if dt == torch.bfloat16 else torch.int32))
+        assert not bool(bad.any()), f"launch {i} differs at {bad.nonzero()[:4].tolist()}"
