@@ -43,8 +43,9 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
-    "fgf8 0.2 sm_103a": {
-        "prefill_pair_4096x18432x7168/up.gemm": 295773440,   # profiles/gemm_blockscaled_prefill_up.md
+    "fgf8 0.3 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_up.md
+        "prefill_pair_4096x18432x7168/up.gemm": 167115520 + 127643904,
+        "prefill_pair_4096x18432x7168/down.gemm": 627432192 + 52022784,
     },
 }
 
@@ -147,6 +148,24 @@ def gemm_flops(g):
     raise TypeError(g)
 
 
+def gemm_bytes(g):
+    """Algorithmic DRAM bytes of one GEMM launch: E4M3 operands, FP32 scales, output."""
+    from fine_grained_fp8_weight_b300.workloads import Dense, Grouped, Wgrad
+    if isinstance(g, Dense):
+        M, K = g.A.shape
+        N = g.B.shape[0]
+        return M * K + N * K + 4 * (M * K // 128 + ((N + 127) // 128) * (K // 128)) + 2 * M * N
+    if isinstance(g, Grouped):
+        M, K = g.A.shape
+        E, N, _ = g.B.shape
+        return M * K + E * N * K + 4 * (M * K // 128 + E * ((N + 127) // 128) * (K // 128)) + 2 * M * N
+    if isinstance(g, Wgrad):
+        T, N = g.dY.shape
+        K = g.X.shape[1]
+        return T * N + T * K + 4 * (T // 128) * (N + K) + 4 * N * K
+    raise TypeError(g)
+
+
 class DevicePath:
     """The step on device buffers: every op is one C-ABI call on one stream."""
 
@@ -219,6 +238,8 @@ class DevicePath:
                                                                             out=C),
                                  gemm_flops(g)))
         self.gemm_flops = sum(w for k, _, _, w in self.ops if k == "gemm")
+        self.gemm_bytes = {f"{g.name}.{'grouped_gemm' if isinstance(g, Grouped) else 'gemm'}": gemm_bytes(g)
+                           for g in work.gemms}
 
     def step(self, events=None):
         for i, (_, _, fn, _) in enumerate(self.ops):
@@ -290,6 +311,9 @@ def run_device(args, rank, world, local_rank):
     # Per-kernel device time: each op captured alone and replayed, one event
     # pair per replay, with an untimed write of a buffer larger than L2 in
     # between so that no op reads inputs left in L2 by its previous replay.
+    # A short device-side sleep before the first event keeps the GPU busy
+    # while the host submits the event and the replay, so the interval holds
+    # the op alone and not the host's submission latency.
     flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
     per_op = {}
     reps = max(3, min(args.op_reps, args.steps))
@@ -305,6 +329,7 @@ def run_device(args, rank, world, local_rank):
         g.replay()
         for e0, e1 in ev:
             flush.fill_(1.0)
+            torch.cuda._sleep(200_000)
             e0.record()
             g.replay()
             e1.record()
@@ -325,6 +350,13 @@ def run_device(args, rank, world, local_rank):
     gemm_ops = [(per_op[name]["ms"], name, w) for kind, name, _, w in path.ops if kind == "gemm"]
     dom_ms, dom_name, dom_flops = max(gemm_ops)
     gemm_ach = dom_flops / (dom_ms * 1e-3) / 1e12
+    dom_bytes = path.gemm_bytes[dom_name]
+    # below the ridge point (peak FLOP/s over peak bytes/s) the launch is bound by HBM
+    hbm_bound = dom_flops / dom_bytes < fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    for kind, name, _, w in path.ops:
+        if kind == "gemm":
+            per_op[name]["GB/s"] = round(path.gemm_bytes[name] / (per_op[name]["ms"] * 1e-3) / 1e9, 1)
+            per_op[name]["frac_hbm"] = round(per_op[name]["GB/s"] / peaks["hbm_gbs"], 4)
     version = fg.lib().fgf8_version().decode()
     traffic = MEASURED_TRAFFIC.get(version, {}).get(f"{work.name}/{dom_name}")
     q_bytes = sum(w for k, _, _, w in path.ops if k == "quant")
@@ -338,12 +370,19 @@ def run_device(args, rank, world, local_rank):
                    "gemms": [n for k, n, _, _ in path.ops if k == "gemm"],
                    "l2": "no flush: each step reads inputs larger than the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_ach / fp8_peak, 4), "traffic": traffic,
-                     "kernel": f"gemm_blockscaled_kernel ({dom_name}, {version})",
-                     "algorithmic_flops_per_launch": dom_flops,
-                     "peak_note": f"fp8 = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
-                                  f"{peaks['bf16_tflops']} TFLOP/s (sustained bf16 {peaks['bf16_tflops_sustained']})"},
+        "roofline": ({"bound": "hbm", "achieved": per_op[dom_name]["GB/s"], "peak": peaks["hbm_gbs"],
+                      "unit": "GB/s", "frac": per_op[dom_name]["frac_hbm"], "traffic": traffic,
+                      "kernel": f"{'gemm_smallm_kernel' if hbm_bound else 'gemm_blockscaled_kernel'} "
+                                f"({dom_name}, {version})",
+                      "algorithmic_bytes_per_launch": dom_bytes,
+                      "peak_note": f"{peaks['source']} HBM copy bandwidth"}
+                     if hbm_bound else
+                     {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp8_peak, 1),
+                      "unit": "TFLOP/s", "frac": round(gemm_ach / fp8_peak, 4), "traffic": traffic,
+                      "kernel": f"gemm_blockscaled_kernel ({dom_name}, {version})",
+                      "algorithmic_flops_per_launch": dom_flops,
+                      "peak_note": f"fp8 = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
+                                   f"{peaks['bf16_tflops']} TFLOP/s (sustained bf16 {peaks['bf16_tflops_sustained']})"}),
         "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "peak_hbm_gbs": peaks["hbm_gbs"],
                      "frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
         "kernels": per_op,
