@@ -183,14 +183,20 @@ __global__ void __launch_bounds__(kTileThreads)
                           uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds,
                           uint8_t *__restrict__ qT, float *__restrict__ sT, int64_t ldsT)
 {
-    __shared__ float colmax[kTileThreads / 32][128];
+    // Thread (c16, g) owns channels 8*c16 .. +7 and tokens 8*g .. +7 of the
+    // 128 x 128 tile.  A warp covers 8 channel octets x 4 token octets, so a
+    // transposed store writes 8 channel rows x 32 contiguous bytes (whole
+    // sectors) and a load reads 4 token rows x 128 bytes.
+    __shared__ float colmax[4][8 * 16];     // [token block][j * 16 + c16]
+    __shared__ float rowmax[2][128];        // [channel half][token]
     const int64_t kb = blockIdx.x;          // channel group
     const int64_t tb = blockIdx.y;          // token group
     const int64_t m0 = tb * 128;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int c16 = tid & 15;               // channels 8*c16 .. 8*c16+7 of the group
-    const int g = tid >> 4;                 // tokens 8*g .. 8*g+7 of the group
+    const int cb = warp & 1, gb = warp >> 1;
+    const int c16 = cb * 8 + (lane & 7);
+    const int g = gb * 4 + (lane >> 3);
     const int64_t tok0 = m0 + 8 * g;
     const bool present = tok0 < M;          // all 8 or none (M % 16 == 0)
 
@@ -202,21 +208,38 @@ __global__ void __launch_bounds__(kTileThreads)
     }
 
     // --- column groups (128x1): the transposed output
+    if (qT != nullptr) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float a = 0.0f;
+        for (int j = 0; j < 8; ++j) {
+            float a = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(bf16_lane(raw[i], j)));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
-        if (lane < 16) colmax[warp][c16 * 8 + j] = a;
+            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(bf16_lane(raw[i], j)));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+            if (lane < 8) colmax[gb][j * 16 + c16] = a;
+        }
+    }
+    // --- row groups (1x128): this warp's 64 channels, then the partner warp's
+    float rmax[8];
+    if (q != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float f[8];
+            bf16x8_to_f32(raw[i], f);
+            float a = amax8(f);
+#pragma unroll
+            for (int o = 4; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            rmax[i] = a;
+            if ((lane & 7) == 0) rowmax[cb][8 * g + i] = a;
+        }
     }
     __syncthreads();
     if (qT != nullptr) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            float a = colmax[0][c16 * 8 + j];
+            float a = colmax[0][j * 16 + c16];
 #pragma unroll
-            for (int w = 1; w < kTileThreads / 32; ++w) a = fmaxf(a, colmax[w][c16 * 8 + j]);
+            for (int w = 1; w < 4; ++w) a = fmaxf(a, colmax[w][j * 16 + c16]);
             const float sc = __fdiv_rn(a, kE4M3Max);
             if (g == 0) sT[tb * ldsT + kb * 128 + c16 * 8 + j] = sc;
             if (present) {
@@ -227,17 +250,13 @@ __global__ void __launch_bounds__(kTileThreads)
             }
         }
     }
-
-    // --- row groups (1x128), from the same registers
     if (q != nullptr) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float f[8];
-            bf16x8_to_f32(raw[i], f);
-            float a = amax8(f);
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float a = fmaxf(rmax[i], rowmax[cb ^ 1][8 * g + i]);
             if (present) {
+                float f[8];
+                bf16x8_to_f32(raw[i], f);
                 const float sc = __fdiv_rn(a, kE4M3Max);
                 *reinterpret_cast<uint2 *>(q + (tok0 + i) * K + kb * 128 + c16 * 8) = encode8(f, make_divisor(sc));
                 if (c16 == 0) s[kb * lds + tok0 + i] = sc;
