@@ -508,6 +508,22 @@ def profile_gemm(args):
     print(json.dumps({"gemm": g.name, "ms": ms, "TFLOP/s": gemm_flops(g) / (ms * 1e-3) / 1e12}))
 
 
+def profile_op(args):
+    """Run the workload's ops once, then the named op four more times (for ncu
+    captures of a single kernel; `-k`/`-s`/`-c` select the launches)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    path = DevicePath(make_workload(args.workload), dev)
+    ops = {name: fn for _, name, fn, _ in path.ops}
+    if args.profile_op not in ops:
+        raise SystemExit(f"unknown op {args.profile_op}; ops of this workload: {sorted(ops)}")
+    path.step()
+    for _ in range(4):
+        ops[args.profile_op]()
+    torch.cuda.synchronize()
+    print(json.dumps({"profiled_op": args.profile_op, "workload": args.workload}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,14 +538,18 @@ def main():
     ap.add_argument("--op-reps", type=int, default=20)
     ap.add_argument("--profile-gemm", action="store_true")
     ap.add_argument("--gemm-index", type=int, default=0)
+    ap.add_argument("--profile-op", default=None, help="run one op of the workload repeatedly (for ncu)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.warmup < 3 and not args.profile_gemm:
+    if args.warmup < 3 and not (args.profile_gemm or args.profile_op):
         print("note: fewer than 3 warm-up steps do not make a valid measurement", file=sys.stderr)
     if args.profile_gemm:
         profile_gemm(args)
+        return
+    if args.profile_op:
+        profile_op(args)
         return
     if args.impl == "reference":
         res = run_reference(args, rank, world)

@@ -141,6 +141,15 @@ def quant_w_128x128(w_bits: np.ndarray):
     return q, s
 
 
+def quant_w_128x128_t(w_bits: np.ndarray):
+    """The 128x128 block quantization of W^T (W: BF16 bits [N, K]), i.e. the B
+    operand of the data-gradient GEMM dX = dY * W, whose inner dimension is N.
+    It is the 128x128 rule applied to the transposed matrix, literally.
+    Returns (qT [K, N] uint8, sT [N/128, round_up(K/128, 4)] float32) with
+    sT[nb, kb] the scale of the block of rows nb*128.. and columns kb*128.. of W."""
+    return quant_w_128x128(np.ascontiguousarray(np.asarray(w_bits, np.uint16).T))
+
+
 def gemm_blockscaled(A, sa, B, sb, bkind: int = 0, rows=None):
     """Binary64 reference of C = A_hat * B_hat^T and the magnitude sum S.
 

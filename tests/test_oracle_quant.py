@@ -194,3 +194,32 @@ def test_block_scale_is_max_of_row_scales():
     for nb in range(3):
         for kb in range(2):
             assert sw[kb, nb] == sr[kb, nb * 128:min(330, nb * 128 + 128)].max()
+
+
+# --- the transposed weight operand of the data-gradient GEMM (dX = dY * W) ---
+
+
+@pytest.mark.parametrize("N,K", [(256, 384), (384, 128), (128, 640)])
+def test_transposed_weight_blocks_commute_with_transposition(N, K):
+    # A 128x128 block of W^T holds the elements of one block of W: same amax,
+    # same scale, same codes -- quantizing W^T must give the transpose of the
+    # quantized W.  N != K so that a swapped index or leading dimension shows.
+    rng = np.random.default_rng(N * 7 + K)
+    w = _random_bf16(rng, (N, K), 0.02, 0.01, 50.0)
+    q, s = oracle.quant_w_128x128(w)
+    qT, sT = oracle.quant_w_128x128_t(w)
+    assert qT.shape == (K, N)
+    assert np.array_equal(qT, q.T)
+    assert np.array_equal(sT[:, : K // 128], s[:, : N // 128].T)
+
+
+def test_transposed_weight_block_closed_form():
+    # blocks built from exact E4M3 values x 2^j: the scale of block (nb, kb) is
+    # 2^j[nb, kb] and the codes are the construction's, read transposed
+    rng = np.random.default_rng(11)
+    bits, c, j = _exact_tensor(rng, 256, 384, 128, 128)
+    qT, sT = oracle.quant_w_128x128_t(bits)
+    assert np.array_equal(qT, c.T)
+    for nb in range(2):
+        for kb in range(3):
+            assert sT[nb, kb] == np.float32(2.0 ** j[nb, kb])
