@@ -133,15 +133,19 @@ def make_workload(name):
         return wl.moe_grouped()
     if name == "wgrad":
         return wl.wgrad()
+    if name == "dgrad":
+        return wl.dgrad()
     if name == "tiny":
         return wl.tiny()
     raise SystemExit(f"unknown workload {name}")
 
 
 def gemm_flops(g):
-    from fine_grained_fp8_weight_b300.workloads import Dense, Grouped, Wgrad
+    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Wgrad
     if isinstance(g, Dense):
         return 2.0 * g.A.shape[0] * g.B.shape[0] * g.A.shape[1]
+    if isinstance(g, Dgrad):
+        return 2.0 * g.dY.shape[0] * g.W.shape[1] * g.dY.shape[1]
     if isinstance(g, Grouped):
         return 2.0 * float(g.counts.sum()) * g.B.shape[1] * g.A.shape[1]
     if isinstance(g, Wgrad):
@@ -151,11 +155,15 @@ def gemm_flops(g):
 
 def gemm_bytes(g):
     """Algorithmic DRAM bytes of one GEMM launch: E4M3 operands, FP32 scales, output."""
-    from fine_grained_fp8_weight_b300.workloads import Dense, Grouped, Wgrad
+    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Wgrad
     if isinstance(g, Dense):
         M, K = g.A.shape
         N = g.B.shape[0]
         return M * K + N * K + 4 * (M * K // 128 + ((N + 127) // 128) * (K // 128)) + 2 * M * N
+    if isinstance(g, Dgrad):
+        T, N = g.dY.shape
+        K = g.W.shape[1]
+        return T * N + K * N + 4 * (T * N // 128 + (N // 128) * (K // 128)) + 2 * T * K
     if isinstance(g, Grouped):
         M, K = g.A.shape
         E, N, _ = g.B.shape
@@ -174,7 +182,7 @@ class DevicePath:
         import torch
         import fine_grained_fp8_weight_b300 as fg
         from fine_grained_fp8_weight_b300 import workloads as wl
-        from fine_grained_fp8_weight_b300.workloads import Dense, Grouped, Wgrad
+        from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Wgrad
         self.fg, self.torch, self.dev = fg, torch, dev
         self.ops = []          # (kind, name, callable, bytes or flops)
         self.inputs = []       # (host numpy bits, device tensor) for the end-to-end leg
@@ -217,6 +225,25 @@ class DevicePath:
                 self.ops.append(("gemm", f"{g.name}.grouped_gemm",
                                  lambda st=st, C=C, mi=mi: fg.fp8_grouped_gemm_blockscaled(
                                      st["a"][0], st["a"][1], st["b"][0], st["b"][1], mi, out=C),
+                                 gemm_flops(g)))
+            elif isinstance(g, Dgrad):
+                dY = wl.bf16_bits_to_torch(g.dY).to(dev)
+                W = wl.bf16_bits_to_torch(g.W).to(dev)
+                self.inputs += [(g.dY, dY), (g.W, W)]
+                T, N = dY.shape
+                K = W.shape[1]
+                st = {}
+                C = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+                self.outputs.append(C)
+                self.ops.append(("quant", f"{g.name}.quant_dY_1x128",
+                                 lambda dY=dY, st=st: st.update(a=fg.fp8_quant_act_1x128(dY)),
+                                 T * N * 3 + T * N // 32))
+                self.ops.append(("quant", f"{g.name}.quant_wT_128x128",
+                                 lambda W=W, st=st: st.update(b=fg.fp8_quant_w_128x128_t(W)),
+                                 N * K * 3 + (N // 128) * (K // 128) * 4))
+                self.ops.append(("gemm", f"{g.name}.gemm",
+                                 lambda st=st, C=C: fg.fp8_gemm_blockscaled(st["a"][0], st["a"][1], st["b"][0],
+                                                                            st["b"][1], out=C),
                                  gemm_flops(g)))
             elif isinstance(g, Wgrad):
                 dY = wl.bf16_bits_to_torch(g.dY).to(dev)
@@ -435,10 +462,18 @@ def oracle_sample(work, rows, blocks):
     rows x (128*blocks) block of the output in binary64.  Returns
     (GEMM FLOPs of the sample, seconds)."""
     import oracle
-    from fine_grained_fp8_weight_b300.workloads import Dense
+    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad
     flops = 0.0
     t = time.perf_counter()
     for g in work.gemms:
+        if isinstance(g, Dgrad):
+            N, K = g.W.shape
+            kb = min(blocks, K // 128)
+            qa, sa = oracle.quant_act_1x128(np.ascontiguousarray(g.dY[:rows]))
+            qb, sb = oracle.quant_w_128x128_t(np.ascontiguousarray(g.W[:, :kb * 128]))
+            oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
+            flops += 2.0 * qa.shape[0] * qb.shape[0] * N
+            continue
         if not isinstance(g, Dense):
             continue
         N, K = g.B.shape
@@ -530,7 +565,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "moe", "wgrad", "tiny"])
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "moe", "wgrad", "dgrad", "tiny"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=16)

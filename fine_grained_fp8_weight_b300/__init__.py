@@ -40,7 +40,7 @@ STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED
 
 # Every symbol declared in include/fgf8.h and include/fgf8_testing.h.
 EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
-            "fp8_quant_w_128x128_grouped",
+            "fp8_quant_w_128x128_grouped", "fp8_quant_w_128x128_t",
             "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm_blockscaled",
             "fgf8_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div"]
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, P, I64, P, P, I64, P]
         L.fp8_quant_w_128x128.argtypes = [P, I64, I64, I64, P, P, I64, P]
         L.fp8_quant_w_128x128_grouped.argtypes = [P, I32, I64, I64, I64, P, P, I64, P]
+        L.fp8_quant_w_128x128_t.argtypes = [P, I64, I64, I64, P, P, I64, P, P, I64, P]
         L.fp8_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, ctypes.c_int, P, I64, ctypes.c_int,
                                            I64, I64, I64, P, SZ, P]
         L.fp8_gemm_blockscaled_noalloc.argtypes = [P, P, I64, P, P, I64, ctypes.c_int, P, I64, ctypes.c_int,
@@ -155,6 +156,25 @@ def fp8_quant_w_128x128(w: torch.Tensor):
     st = lib().fp8_quant_w_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), _ptr(s), s.shape[1], _stream(w.device))
     _check(st, "fp8_quant_w_128x128")
     return q, s
+
+
+def fp8_quant_w_128x128_t(w: torch.Tensor, forward: bool = False):
+    """128x128 weight quantization written as W^T for the data-gradient GEMM.
+    w: BF16 [N, K], N % 128 == 0.  Returns (qT [K, N], sT [N/128, round_up(K/128, 4)])
+    and, with forward=True, also (q [N, K], s) as fp8_quant_w_128x128."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1
+    N, K = w.shape
+    qT = torch.empty((K, N), dtype=torch.uint8, device=w.device)
+    sT = torch.empty((N // 128, round_up(K // 128, 4)), dtype=torch.float32, device=w.device)
+    q = s = None
+    if forward:
+        q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+        s = torch.empty((K // 128, round_up(N // 128, 4)), dtype=torch.float32, device=w.device)
+    st = lib().fp8_quant_w_128x128_t(_ptr(w), N, K, w.stride(0), _ptr(qT), _ptr(sT), sT.shape[1],
+                                     _ptr(q) if forward else None, _ptr(s) if forward else None,
+                                     s.shape[1] if forward else 0, _stream(w.device))
+    _check(st, "fp8_quant_w_128x128_t")
+    return (qT, sT, q, s) if forward else (qT, sT)
 
 
 def fp8_quant_w_128x128_grouped(w: torch.Tensor):

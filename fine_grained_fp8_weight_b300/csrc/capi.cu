@@ -129,6 +129,23 @@ fgf8_status fp8_quant_w_128x128_grouped(const void *w, int32_t num_experts, int6
         fgf8::launch_quant_w(w, N, K, ldw, q, s, lds, num_experts, static_cast<cudaStream_t>(stream)));
 }
 
+fgf8_status fp8_quant_w_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *qT, float *sT,
+                                  int64_t ldsT, uint8_t *q, float *s, int64_t lds, void *stream)
+{
+    if (N < 0 || K <= 0) return FGF8_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0) return FGF8_OK;                 // empty input: nothing to read or write
+    if (w == nullptr || qT == nullptr || sT == nullptr || ldw < K) return FGF8_ERR_INVALID_ARG;
+    if (ldsT < K / 128 || ldsT % 4 != 0) return FGF8_ERR_INVALID_ARG;
+    if ((q == nullptr) != (s == nullptr)) return FGF8_ERR_INVALID_ARG;
+    if (q != nullptr && (lds < N / 128 || lds % 4 != 0)) return FGF8_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || ldw % 8 != 0 || !aligned(qT, 16) || !aligned(sT, 16)) return FGF8_ERR_MISALIGNED;
+    if (q != nullptr && (!aligned(q, 16) || !aligned(s, 16))) return FGF8_ERR_MISALIGNED;
+    fgf8_status st = current_device(nullptr);
+    if (st != FGF8_OK) return st;
+    return from_cuda(fgf8::launch_quant_w_t(w, N, K, ldw, qT, sT, ldsT, q, s, lds, static_cast<cudaStream_t>(stream)));
+}
+
 size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts)
 {
     return fgf8::gemm_workspace_bytes(M, N, K, num_experts, 0);

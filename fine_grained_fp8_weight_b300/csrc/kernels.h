@@ -16,6 +16,8 @@ cudaError_t launch_scaled_div_selftest(const float *x, const float *s, int64_t n
                                        cudaStream_t stream);
 cudaError_t launch_quant_w(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, float *s, int64_t lds,
                            int32_t num_experts, cudaStream_t stream);
+cudaError_t launch_quant_w_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *qT, float *sT, int64_t ldsT,
+                             uint8_t *q, float *s, int64_t lds, cudaStream_t stream);
 
 struct GemmArgs {
     const uint8_t *A;

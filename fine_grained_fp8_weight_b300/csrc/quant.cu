@@ -327,6 +327,76 @@ __global__ void __launch_bounds__(kBlockThreads)
     }
 }
 
+// ------------------------------------------------------------------------
+// 128x128 weight blocks written transposed: W^T, the B operand of the
+// data-gradient GEMM dX = dY * W (inner dimension N).  A block of W^T holds the
+// elements of one block of W, so scale and codes are those of the forward
+// layout, transposed; the forward layout can be written in the same pass.
+// Staging as in quant_w_block_kernel; afterwards each thread encodes an 8 x 8
+// sub-block, and a warp (8 column octets x 4 row octets) writes 8 rows of W^T
+// x 32 contiguous bytes per store.
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(kBlockThreads)
+    quant_w_block_t_kernel(const __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                           uint8_t *__restrict__ qT, float *__restrict__ sT, int64_t ldsT,
+                           uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds)
+{
+    __shared__ __align__(16) uint4 tile[128 * 16];
+    __shared__ float red[kBlockThreads / 32];
+    const int64_t kb = blockIdx.x;
+    const int64_t nb = blockIdx.y;
+    const int64_t n0 = nb * 128;            // N % 128 == 0: every block is full
+    const int tid = threadIdx.x;
+
+#pragma unroll
+    for (int i = 0; i < kBlockChunks; ++i) {
+        const int c = tid + i * kBlockThreads;
+        cp_async_16(&tile[c], w + (n0 + (c >> 4)) * ldw + kb * 128 + (c & 15) * 8);
+    }
+    cp_async_wait_all();
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kBlockChunks; ++i) {
+        float f[8];
+        bf16x8_to_f32(tile[tid + i * kBlockThreads], f);
+        a = fmaxf(a, amax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((tid & 31) == 0) red[tid >> 5] = a;
+    __syncthreads();                        // also publishes every thread's staged chunks
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kBlockThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    const float sc = __fdiv_rn(amax, kE4M3Max);
+    const Divisor dv = make_divisor(sc);
+    if (tid == 0) {
+        sT[nb * ldsT + kb] = sc;
+        if (s != nullptr) s[kb * lds + nb] = sc;
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c8 = (warp & 1) * 8 + (lane & 7);     // columns 8*c8 .. +7 of the block (K direction)
+    const int r8 = (warp >> 1) * 4 + (lane >> 3);   // rows 8*r8 .. +7 (N direction)
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) raw[i] = tile[(8 * r8 + i) * 16 + c8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float col[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) col[i] = bf16_lane(raw[i], j);
+        *reinterpret_cast<uint2 *>(qT + (kb * 128 + 8 * c8 + j) * N + n0 + 8 * r8) = encode8(col, dv);
+    }
+    if (q != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float f[8];
+            bf16x8_to_f32(raw[i], f);
+            *reinterpret_cast<uint2 *>(q + (n0 + 8 * r8 + i) * K + kb * 128 + 8 * c8) = encode8(f, dv);
+        }
+    }
+}
+
 // Test hook: the quotient the encoders use next to CUDA's IEEE division.
 __global__ void scaled_div_selftest_kernel(const float *__restrict__ x, const float *__restrict__ s, int64_t n,
                                            float *__restrict__ fast, float *__restrict__ ieee)
@@ -368,6 +438,16 @@ cudaError_t launch_quant_act_tiles(const void *x, int64_t M, int64_t K, int64_t 
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
     quant_act_tile_kernel<<<grid, kTileThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), M, K, ldx, q,
                                                              s, lds, qT, sT, ldsT);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_w_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *qT, float *sT, int64_t ldsT,
+                             uint8_t *q, float *s, int64_t lds, cudaStream_t stream)
+{
+    const dim3 grid((unsigned)(K / 128), (unsigned)(N / 128));
+    if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+    quant_w_block_t_kernel<<<grid, kBlockThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), N, K, ldw, qT,
+                                                               sT, ldsT, q, s, lds);
     return cudaGetLastError();
 }
 

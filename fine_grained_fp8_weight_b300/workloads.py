@@ -91,6 +91,16 @@ class Wgrad:
 
 
 @dataclass
+class Dgrad:
+    """dX[T,K] = dY[T,N] * W[N,K]: dY quantized 1x128 along N, W as W^T in
+    128x128 blocks (the GEMM's B operand [K,N])."""
+    name: str
+    dY: np.ndarray
+    W: np.ndarray
+    out: str = "bf16"
+
+
+@dataclass
 class Workload:
     name: str
     gemms: list = field(default_factory=list)
@@ -179,3 +189,12 @@ def wgrad(seed: int = 4, T: int = 8192, N: int = 7168, K: int = 2048) -> Workloa
     dY = bf16_normal(rng, (T, N), 1.0, 0.001, 50.0)
     X = bf16_normal(rng, (T, K), 1.0, 0.001, 50.0)
     return Workload(f"wgrad_{N}x{K}x{T}", [Wgrad("wgrad", dY, X)])
+
+
+def dgrad(seed: int = 5, T: int = 4096, N: int = 18432, K: int = 7168) -> Workload:
+    """Data gradient through the prefill up-projection: dY [T,N] N(0,1) with
+    0.1% outliers x50, W [N,K] N(0,0.02); dX = dY W in bf16."""
+    rng = np.random.default_rng(seed)
+    dY = bf16_normal(rng, (T, N), 1.0, 0.001, 50.0)
+    W = bf16_normal(rng, (N, K), 0.02)
+    return Workload(f"dgrad_{T}x{K}x{N}", [Dgrad("dgrad", dY, W)])

@@ -125,6 +125,27 @@ fgf8_status fp8_quant_w_128x128_grouped(const void *w, int32_t num_experts, int6
                                         int64_t ldw, uint8_t *q, float *s, int64_t lds, void *stream);
 
 /*
+ * fp8_quant_w_128x128_t -- the 128x128 block quantization of W written as W^T,
+ * the B operand of the data-gradient GEMM dX = dY * W (whose inner dimension
+ * is N), for FP8 Dgrad ([dssusan] E4M3 passage: E4M3 on the Dgrad operands;
+ * [why-be] transposed-read passage: the backward pass reads transposed
+ * copies).  A 128x128 block of W^T holds the elements of one block of W, so
+ * its scale and codes equal fp8_quant_w_128x128's, transposed; the forward
+ * layout (q, s) may be written in the same pass.
+ *
+ *   w  : BF16 [N][ldw], ldw >= K, ldw % 8 == 0, 16-byte aligned.
+ *        N % 128 == 0 and K % 128 == 0 (the transposed operand's inner
+ *        dimension is N); N == 0 is a no-op that reads no pointer.
+ *   qT : E4M3 [K][N] (row k holds column k of W), 16-byte aligned.
+ *   sT : float [N/128][ldsT], sT[nb*ldsT + kb] = scale of rows nb*128.. and
+ *        columns kb*128.. of W; ldsT >= K/128, ldsT % 4 == 0.  This is the sb
+ *        of fp8_gemm_blockscaled with B = qT (BLOCK128 kind).
+ *   q, s : optional (both NULL or both set), as fp8_quant_w_128x128.
+ */
+fgf8_status fp8_quant_w_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *qT, float *sT,
+                                  int64_t ldsT, uint8_t *q, float *s, int64_t lds, void *stream);
+
+/*
  * fp8_gemm_blockscaled -- C = A_hat * B_hat^T with per-group scales along the
  * inner dimension K ([dssusan] inner-dimension and E4M3 passages).  Each
  * 128-wide K partial product P = sum_{k in group} qa*qb is formed on the

@@ -9,7 +9,7 @@ import torch
 import oracle
 import fine_grained_fp8_weight_b300 as fg
 from fine_grained_fp8_weight_b300 import workloads as wl
-from tests.gpu_util import DEV, assert_within_bound, bf16_out_to_f64, ensure_built
+from tests.gpu_util import DEV, assert_within_bound, bf16_out_to_f64, dev_bf16, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -236,3 +236,31 @@ def test_repeated_launches_bitwise_identical(M, N, K, bkind, out):
         bad = (o.view(torch.int16 if dt == torch.bfloat16 else torch.int32)
                != outs[0].view(torch.int16 if dt == torch.bfloat16 else torch.int32))
         assert not bool(bad.any()), f"launch {i} differs at {bad.nonzero()[:4].tolist()}"
+
+
+# --- data gradient dX = dY * W: A = dY (1x128 along N), B = W^T (128x128) ---
+
+
+@pytest.mark.parametrize("T,N,K", [(200, 384, 256), (256, 1024, 512), (1000, 256, 384)])
+def test_dgrad_small(T, N, K):
+    rng = np.random.default_rng(T + N * 3 + K)
+    dY = wl.bf16_normal(rng, (T, N), 1.0, 0.001, 50.0)
+    W = wl.bf16_normal(rng, (N, K), 0.02)
+    qa, sa = oracle.quant_act_1x128(dY)
+    qT, sT = fg.fp8_quant_w_128x128_t(dev_bf16(W))
+    C = fg.fp8_gemm_blockscaled(_d(qa), _d(sa), qT, sT, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rqT, rsT = oracle.quant_w_128x128_t(W)
+    Cr, S = oracle.gemm_blockscaled(qa, sa, rqT, rsT)
+    assert_within_bound(C.cpu().numpy().astype(np.float64), Cr, S, "dgrad")
+
+
+def test_full_size_dgrad_sampled():
+    g = wl.dgrad().gemms[0]
+    qa, sa = oracle.quant_act_1x128(g.dY)
+    rqT, rsT = oracle.quant_w_128x128_t(g.W)
+    C = fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(rqT), _d(rsT))
+    torch.cuda.synchronize()
+    rows = _sample_rows(g.dY.shape[0], 3, 15)
+    Cr, S = oracle.gemm_blockscaled(qa, sa, rqT, rsT, rows=rows)
+    assert_within_bound(bf16_out_to_f64(C)[rows], Cr, S, "dgrad")

@@ -181,3 +181,49 @@ def test_full_size_decode_and_tiny():
     for g in wl.tiny().gemms + wl.decode().gemms[:2]:
         _check_rows(g.A)
     _check_weights(wl.tiny().gemms[0].B)
+
+
+# --- W^T for the data-gradient GEMM (128x128 blocks written transposed) ---
+
+
+def _check_weights_t(bits, forward):
+    N, K = bits.shape
+    out = fg.fp8_quant_w_128x128_t(dev_bf16(bits), forward=forward)
+    rqT, rsT = oracle.quant_w_128x128_t(bits)
+    assert_codes_equal(host(out[0]), rqT)
+    assert_scales_equal(host(out[1]), rsT, K // 128)
+    if forward:
+        rq, rs = oracle.quant_w_128x128(bits)
+        assert_codes_equal(host(out[2]), rq)
+        assert_scales_equal(host(out[3]), rs, N // 128)
+
+
+@pytest.mark.parametrize("N,K,forward", [(128, 128, False), (256, 384, True), (384, 128, False),
+                                         (1024, 640, True), (128, 2048, False)])
+def test_weights_transposed_random(N, K, forward):
+    rng = np.random.default_rng(N * 5 + K)
+    _check_weights_t(wl.bf16_normal(rng, (N, K), 0.02, 0.001, 50.0), forward)
+
+
+def test_weights_transposed_edge_cases():
+    _check_weights_t(_edge_tensor(256, 256), forward=True)
+    _check_weights_t(np.zeros((128, 256), np.uint16), forward=True)
+
+
+def test_weights_transposed_rejects_ragged_n():
+    w = torch.zeros((200, 256), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(fg.FGF8Error, match="UNSUPPORTED_SHAPE"):
+        fg.fp8_quant_w_128x128_t(w)
+
+
+def test_full_size_dgrad_weight():
+    g = wl.dgrad().gemms[0]
+    qT, sT = fg.fp8_quant_w_128x128_t(dev_bf16(g.W))
+    torch.cuda.synchronize()
+    # sampled 128-column blocks of W (= 128-row blocks of W^T), checked whole
+    rng = np.random.default_rng(21)
+    for kb in rng.choice(g.W.shape[1] // 128, size=3, replace=False):
+        cols = slice(int(kb) * 128, int(kb) * 128 + 128)
+        rqT, rsT = oracle.quant_w_128x128_t(np.ascontiguousarray(g.W[:, cols]))
+        assert_codes_equal(host(qT[cols]), rqT)
+        assert_scales_equal(host(sT[:, int(kb):int(kb) + 1]), rsT, 1)
