@@ -200,6 +200,35 @@ def grouped_gemm_blockscaled(A, sa, B, sb, m_indices, rows=None):
     return C, S
 
 
+def masked_grouped_gemm_blockscaled(A, sa, B, sb, counts, rows_per_expert=None):
+    """Masked-layout grouped reference (decode MoE): expert e owns a slot of
+    `cap` token rows, of which the first counts[e] are real.
+    A [E, cap, K] codes, sa [E, K/128, lda_s]; B [E, N, K], sb [E, K/128, ldb_s].
+    Returns C, S of shape [E, cap, N]: for every expert the dense block-scaled
+    GEMM of its real rows with its own weights; rows past the count are NaN
+    (S = 0).  ``rows_per_expert``: optional list of row indices to evaluate
+    within each expert's real rows."""
+    A = np.ascontiguousarray(A, np.uint8)
+    E, cap, K = A.shape
+    N = B.shape[1]
+    C = np.full((E, cap, N), np.nan)
+    S = np.zeros((E, cap, N))
+    for e in range(E):
+        c = int(min(max(int(counts[e]), 0), cap))
+        if c == 0:
+            continue
+        rows = None
+        if rows_per_expert is not None:
+            rows = [r for r in rows_per_expert if r < c]
+            if not rows:
+                continue
+        Ce, Se = gemm_blockscaled(A[e, :c], sa[e], B[e], sb[e], 0, rows=rows)
+        idx = rows if rows is not None else slice(0, c)
+        C[e, idx] = Ce
+        S[e, idx] = Se
+    return C, S
+
+
 def dot_e4m3_exact(a_codes, b_codes) -> int:
     """Exact dot product of two E4M3 code vectors, in units of 2^-18."""
     a = np.ascontiguousarray(a_codes, np.uint8)

@@ -170,3 +170,60 @@ def test_dot_exact_matches_fractions():
         b = rng.choice(FINITE, size=K)
         exact = sum(Fraction(float(T[x])) * Fraction(float(T[y])) for x, y in zip(a, b))
         assert Fraction(oracle.dot_e4m3_exact(a, b), 2 ** 18) == exact
+
+
+def _masked_case(seed, E, cap, N, K, counts):
+    rng = np.random.default_rng(seed)
+    av, A = _int_codes(rng, (E, cap, K))
+    bv, B = _int_codes(rng, (E, N, K))
+    ja = rng.integers(-3, 4, size=(E, K // 128, cap))
+    jb = rng.integers(-3, 4, size=(E, K // 128, (N + 127) // 128))
+    sa = np.zeros((E, K // 128, (cap + 3) // 4 * 4), np.float32)
+    sa[:, :, :cap] = np.exp2(ja)
+    sb = np.zeros((E, K // 128, ((N + 127) // 128 + 3) // 4 * 4), np.float32)
+    sb[:, :, :jb.shape[2]] = np.exp2(jb)
+    return av, A, bv, B, ja, jb, sa, sb
+
+
+def test_masked_grouped_integer_experts():
+    # exact: integer codes, power-of-two scales, sums far below 2^53
+    E, cap, N, K = 3, 48, 144, 256
+    counts = np.array([48, 0, 17], np.int32)
+    av, A, bv, B, ja, jb, sa, sb = _masked_case(31, E, cap, N, K, counts)
+    C, S = oracle.masked_grouped_gemm_blockscaled(A, sa, B, sb, counts)
+    for e in range(E):
+        for m in range(cap):
+            if m >= counts[e]:
+                assert np.all(np.isnan(C[e, m])) and np.all(S[e, m] == 0)
+                continue
+            ref = np.zeros(N)
+            for kb in range(K // 128):
+                part = (bv[e][:, kb * 128:(kb + 1) * 128] @ av[e, m, kb * 128:(kb + 1) * 128]).astype(np.float64)
+                ref += part * 2.0 ** ja[e, kb, m] * np.exp2(np.repeat(jb[e, kb], 128)[:N])
+            assert np.array_equal(C[e, m], ref)
+
+
+def test_masked_grouped_equals_contiguous_grouped():
+    # the masked slots, packed into the contiguous padded layout, must give the
+    # contiguous-layout routine's result row for row (a separate code path)
+    E, cap, N, K = 4, 64, 256, 384
+    counts = np.array([64, 5, 0, 33], np.int32)
+    _, A, _, B, _, _, sa, sb = _masked_case(32, E, cap, N, K, counts)
+    Cm, Sm = oracle.masked_grouped_gemm_blockscaled(A, sa, B, sb, counts)
+    rows, m_idx, sa_c = [], [], []
+    for e in range(E):
+        pad = (int(counts[e]) + 127) // 128 * 128
+        for r in range(pad):
+            rows.append(A[e, r] if r < counts[e] else np.zeros(K, np.uint8))
+            m_idx.append(e if r < counts[e] else -1)
+            sa_c.append(sa[e, :, r] if r < counts[e] else np.zeros(K // 128, np.float32))
+    Ac = np.stack(rows)
+    sac = np.zeros((K // 128, (len(rows) + 3) // 4 * 4), np.float32)
+    sac[:, :len(rows)] = np.stack(sa_c, axis=1)
+    Cc, Sc = oracle.grouped_gemm_blockscaled(Ac, sac, B, sb, np.array(m_idx, np.int32))
+    i = 0
+    for e in range(E):
+        pad = (int(counts[e]) + 127) // 128 * 128
+        for r in range(int(counts[e])):
+            assert np.array_equal(Cm[e, r], Cc[i + r]) and np.array_equal(Sm[e, r], Sc[i + r])
+        i += pad
