@@ -135,13 +135,17 @@ def make_workload(name):
         return wl.wgrad()
     if name == "dgrad":
         return wl.dgrad()
+    if name == "moe_decode":
+        return wl.moe_decode()
     if name == "tiny":
         return wl.tiny()
     raise SystemExit(f"unknown workload {name}")
 
 
 def gemm_flops(g):
-    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Wgrad
+    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Masked, Wgrad
+    if isinstance(g, Masked):
+        return 2.0 * float(g.counts.sum()) * g.B.shape[1] * g.A.shape[2]
     if isinstance(g, Dense):
         return 2.0 * g.A.shape[0] * g.B.shape[0] * g.A.shape[1]
     if isinstance(g, Dgrad):
@@ -155,7 +159,13 @@ def gemm_flops(g):
 
 def gemm_bytes(g):
     """Algorithmic DRAM bytes of one GEMM launch: E4M3 operands, FP32 scales, output."""
-    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Wgrad
+    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Masked, Wgrad
+    if isinstance(g, Masked):
+        E, cap, K = g.A.shape
+        N = g.B.shape[1]
+        live = int((g.counts > 0).sum())      # idle experts' weights are not read
+        return (int(g.counts.sum()) * K + live * N * K + 4 * (E * cap * K // 128 + live * ((N + 127) // 128) * (K // 128))
+                + 2 * int(g.counts.sum()) * N)
     if isinstance(g, Dense):
         M, K = g.A.shape
         N = g.B.shape[0]
@@ -182,7 +192,7 @@ class DevicePath:
         import torch
         import fine_grained_fp8_weight_b300 as fg
         from fine_grained_fp8_weight_b300 import workloads as wl
-        from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Wgrad
+        from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Masked, Wgrad
         self.fg, self.torch, self.dev = fg, torch, dev
         self.ops = []          # (kind, name, callable, bytes or flops)
         self.inputs = []       # (host numpy bits, device tensor) for the end-to-end leg
@@ -225,6 +235,25 @@ class DevicePath:
                 self.ops.append(("gemm", f"{g.name}.grouped_gemm",
                                  lambda st=st, C=C, mi=mi: fg.fp8_grouped_gemm_blockscaled(
                                      st["a"][0], st["a"][1], st["b"][0], st["b"][1], mi, out=C),
+                                 gemm_flops(g)))
+            elif isinstance(g, Masked):
+                E, cap, K = g.A.shape
+                N = g.B.shape[1]
+                A = wl.bf16_bits_to_torch(g.A.reshape(E * cap, K)).to(dev)
+                B = wl.bf16_bits_to_torch(g.B).to(dev)
+                cnt = torch.from_numpy(g.counts).to(dev)
+                self.inputs += [(g.A.reshape(E * cap, K), A), (g.B, B)]
+                st = {}
+                C = torch.empty((E, cap, N), dtype=torch.bfloat16, device=dev)
+                self.outputs.append(C)
+                self.ops.append(("quant", f"{g.name}.quant_act_1x128",
+                                 lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)),
+                                 E * cap * K * 3 + E * cap * K // 32))
+                self.ops.append(("quant", f"{g.name}.quant_w_128x128_grouped",
+                                 lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128_grouped(B)), E * N * K * 3))
+                self.ops.append(("gemm", f"{g.name}.gemm",
+                                 lambda st=st, C=C, cnt=cnt, E=E, cap=cap, K=K: fg.fp8_masked_grouped_gemm_blockscaled(
+                                     st["a"][0].view(E, cap, K), st["a"][1], st["b"][0], st["b"][1], cnt, out=C),
                                  gemm_flops(g)))
             elif isinstance(g, Dgrad):
                 dY = wl.bf16_bits_to_torch(g.dY).to(dev)
@@ -565,7 +594,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "moe", "wgrad", "dgrad", "tiny"])
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "moe", "moe_decode", "wgrad", "dgrad",
+                                                               "tiny"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=16)

@@ -42,7 +42,7 @@ STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED
 EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
             "fp8_quant_w_128x128_grouped", "fp8_quant_w_128x128_t",
             "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm_blockscaled",
-            "fgf8_gemm_workspace_bytes",
+            "fp8_masked_grouped_gemm_blockscaled", "fgf8_gemm_workspace_bytes", "fgf8_masked_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div"]
 
 
@@ -80,6 +80,10 @@ def lib() -> ctypes.CDLL:
                                                    I64, I64, I64, P, SZ, P]
         L.fgf8_gemm_workspace_bytes.argtypes = [I64, I64, I64, I32]
         L.fgf8_gemm_workspace_bytes.restype = SZ
+        L.fp8_masked_grouped_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, P, I32, I64, P, I64, ctypes.c_int,
+                                                          I64, I64, P, SZ, P]
+        L.fgf8_masked_gemm_workspace_bytes.argtypes = [I32, I64, I64, I64]
+        L.fgf8_masked_gemm_workspace_bytes.restype = SZ
         L.fgf8_read_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
         L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
@@ -222,6 +226,29 @@ def fp8_grouped_gemm_blockscaled(A, sa, B, sb, m_indices, out_dtype=torch.bfloat
                                             _ptr(m_indices), E, _ptr(out), out.stride(0), cdt, M, N, K,
                                             _ptr(ws), ws.numel(), _stream(A.device))
     _check(st, "fp8_grouped_gemm_blockscaled")
+    return out
+
+
+def fp8_masked_grouped_gemm_blockscaled(A, sa, B, sb, counts, out_dtype=torch.bfloat16,
+                                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Masked-layout grouped GEMM (decode MoE).  A [E, cap, K] uint8 with sa [K/128, ldsa]
+    (the 1x128 scales of the stacked [E*cap, K] slots), B [E, N, K] with sb [E, K/128, ldsb],
+    counts int32 [E] on the device.  Returns C [E, cap, N]; rows past each expert's count
+    are left as they were in `out`."""
+    E, cap, K = A.shape
+    N = B.shape[1]
+    assert sa.dim() == 2 and sa.stride(1) == 1
+    assert sb.stride(2) == 1 and sb.stride(0) == sb.shape[1] * sb.stride(1)
+    if out is None:
+        out = torch.empty((E, cap, N), dtype=out_dtype, device=A.device)
+    assert out.stride(0) == cap * out.stride(1)
+    cdt = OUT_FP32 if out.dtype == torch.float32 else OUT_BF16
+    need = lib().fgf8_masked_gemm_workspace_bytes(E, cap, N, K)
+    ws = workspace if workspace is not None else workspace_for(A.device, need)
+    st = lib().fp8_masked_grouped_gemm_blockscaled(_ptr(A), _ptr(sa), sa.stride(0), _ptr(B), _ptr(sb), sb.stride(1),
+                                                   _ptr(counts), E, cap, _ptr(out), out.stride(1), cdt, N, K,
+                                                   _ptr(ws), ws.numel(), _stream(A.device))
+    _check(st, "fp8_masked_grouped_gemm_blockscaled")
     return out
 
 

@@ -208,6 +208,45 @@ fgf8_status fp8_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int6
     return from_cuda(fgf8::launch_gemm(a, static_cast<cudaStream_t>(stream), num_sms));
 }
 
+size_t fgf8_masked_gemm_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K)
+{
+    if (num_experts < 1 || cap < 1 || N < 1 || K < 128) return fgf8::kWsHeaderBytes;
+    return fgf8::masked_workspace_bytes(num_experts, cap, N, K);
+}
+
+fgf8_status fp8_masked_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa, const uint8_t *B,
+                                                const float *sb, int64_t ldsb, const int32_t *counts,
+                                                int32_t num_experts, int64_t cap, void *C, int64_t ldc,
+                                                fgf8_out_dtype cdt, int64_t N, int64_t K, void *workspace,
+                                                size_t ws_bytes, void *stream)
+{
+    if (num_experts < 0 || num_experts > 65535) return FGF8_ERR_INVALID_ARG;
+    if (num_experts == 0) return FGF8_OK;                // nothing to read or write
+    if (!A || !sa || !B || !sb || !counts || !C || !workspace) return FGF8_ERR_INVALID_ARG;
+    if (cap < 1 || N < 1 || K < 1) return FGF8_ERR_INVALID_ARG;
+    if (cdt != FGF8_OUT_BF16 && cdt != FGF8_OUT_FP32) return FGF8_ERR_INVALID_ARG;
+    if (cap > 256 || cap % 16 != 0 || K % 128 != 0 || N % 16 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)num_experts * N > INT32_MAX / 2 || (int64_t)num_experts * cap > INT32_MAX / 2 ||
+        (int64_t)num_experts * (K / 128) > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (ldsa < (int64_t)num_experts * cap || ldsa % 4 != 0) return FGF8_ERR_INVALID_ARG;
+    if (ldsb < (N + 127) / 128 || ldsb % 4 != 0) return FGF8_ERR_INVALID_ARG;
+    if (ldc < N) return FGF8_ERR_INVALID_ARG;
+    const int64_t esz = cdt == FGF8_OUT_BF16 ? 2 : 4;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(C, 16) ||
+        !aligned(counts, 4) || (ldc * esz) % 16 != 0 || !aligned(workspace, 256))
+        return FGF8_ERR_MISALIGNED;
+    if (ws_bytes < fgf8::masked_workspace_bytes(num_experts, cap, N, K)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
+    int num_sms = 0;
+    fgf8_status st = current_device(&num_sms);
+    if (st != FGF8_OK) return st;
+    fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, 0, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, cap, N, K,
+                     nullptr, num_experts, workspace, ws_bytes};
+    a.counts = counts;
+    a.cap = cap;
+    return from_cuda(fgf8::launch_masked(a, static_cast<cudaStream_t>(stream), num_sms));
+}
+
 // ---------------------------------------------------------------------------
 // Allocation-free GEMM entry point.  Its scratch (the device status word of the
 // GEMM kernel) lives in this file-scope device array instead of a workspace

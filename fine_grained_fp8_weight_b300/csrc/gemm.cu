@@ -416,9 +416,15 @@ struct SmallParams {
     int32_t KB, S, n_tiles;
     void *C;
     int64_t ldc;
-    float *partials;          // [n_tiles][S][NT][128]
-    uint32_t *tickets;        // [n_tiles], zero between calls
+    float *partials;          // [experts][n_tiles][S][NT][128]
+    uint32_t *tickets;        // [experts][n_tiles], zero between calls
     DeviceStatus *status;
+    // masked grouped layout (decode MoE): expert e owns token rows
+    // e*cap .. e*cap+cap-1 of A and C (and those columns of sa) and weight
+    // rows e*N .. of B; only its first counts[e] tokens are real.  Dense:
+    // counts == nullptr, cap == M.
+    const int32_t *counts;
+    int64_t cap;
 };
 
 template <int NT, int STAGES, int SC>
@@ -469,8 +475,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
-    const int32_t tile = blockIdx.x / p.S;       // 128 weight rows
-    const int32_t split = blockIdx.x - tile * p.S;
+    const int32_t per_expert = p.n_tiles * p.S;
+    const int32_t e = blockIdx.x / per_expert;   // expert (0 for a dense GEMM)
+    const int32_t rem = blockIdx.x - e * per_expert;
+    const int32_t tile = rem / p.S;              // 128 weight rows
+    const int32_t split = rem - tile * p.S;
+    const int32_t et = e * p.n_tiles + tile;     // (expert, weight tile)
+    int64_t m_real = p.M;                        // token columns that are written
+    if (p.counts != nullptr) {
+        int32_t c = __ldg(p.counts + e);
+        c = c < 0 ? 0 : (c > p.cap ? (int32_t)p.cap : c);
+        if (c == 0) return;                      // idle expert: its weights are not even read
+        m_real = c;
+    }
     const int32_t kb0 = (int32_t)((int64_t)split * p.KB / p.S);
     const int32_t kb1 = (int32_t)((int64_t)(split + 1) * p.KB / p.S);
     const int32_t ngroups = kb1 - kb0;
@@ -515,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + L::x_bytes));
-                tma_load_2d(sm_w + s * L::w_bytes, &tmW, &full[s], (kb0 + g) * BK, tile * BM);
-                tma_load_2d(sm_x + s * L::x_bytes, &tmX, &full[s], (kb0 + g) * BK, 0);
+                tma_load_2d(sm_w + s * L::w_bytes, &tmW, &full[s], (kb0 + g) * BK, (int32_t)(e * p.N) + tile * BM);
+                tma_load_2d(sm_x + s * L::x_bytes, &tmX, &full[s], (kb0 + g) * BK, (int32_t)(e * p.cap));
             }
         }
         __syncwarp();
@@ -532,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(NT * 4 + 16));
-                tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], 0, kb0 + g);
-                tma_load_2d(sm_sb + j * 32, &tmSB, &sc_full[j], tile & ~3, kb0 + g);
+                tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + g);
+                tma_load_2d(sm_sb + j * 32, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + g);
             }
         }
         __syncwarp();
@@ -626,16 +643,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < 2; ++h) {
                         const int64_t m = col0 + 2 * i + h;
                         const float v = h ? acc[i].y : acc[i].x;
-                        if (m < p.M) {
-                            if (OUT_F32) static_cast<float *>(p.C)[m * p.ldc + n] = v;
-                            else static_cast<__nv_bfloat16 *>(p.C)[m * p.ldc + n] = __float2bfloat16_rn(v);
+                        if (m < m_real) {
+                            const int64_t row = e * p.cap + m;
+                            if (OUT_F32) static_cast<float *>(p.C)[row * p.ldc + n] = v;
+                            else static_cast<__nv_bfloat16 *>(p.C)[row * p.ldc + n] = __float2bfloat16_rn(v);
                         }
                     }
                 }
             }
         } else if (p.S > 1) {
             // this split's partial: [column][weight row], one 128-byte row per warp store
-            float *part = p.partials + ((int64_t)tile * p.S + split) * NT * BM;
+            float *part = p.partials + ((int64_t)et * p.S + split) * NT * BM;
             if (ok) {
 #pragma unroll
                 for (int i = 0; i < COLS / 2; ++i) {
@@ -647,9 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // all eight promotion warps have written; none gave up?
             const bool all_ok = named_barrier_and(1, kEpiWarps * 32, ok && !*abort_flag);
             if (all_ok && threadIdx.x == kEpiWarp0 * 32) {
-                const uint32_t ticket = atomicAdd(p.tickets + tile, 1u);
+                const uint32_t ticket = atomicAdd(p.tickets + et, 1u);
                 const int last = ticket == (uint32_t)p.S - 1;
-                if (last) p.tickets[tile] = 0u;                 // ready for the next call
+                if (last) p.tickets[et] = 0u;                   // ready for the next call
                 flags[1] = last;
             }
             named_barrier_sync(1, kEpiWarps * 32);
@@ -659,21 +677,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 constexpr int kRedUnroll = 4;
                 constexpr int E4 = NT * BM / 4;                 // float4 per partial
-                const float4 *base = reinterpret_cast<const float4 *>(p.partials + (int64_t)tile * p.S * NT * BM);
+                const float4 *base = reinterpret_cast<const float4 *>(p.partials + (int64_t)et * p.S * NT * BM);
                 const int t = (int)threadIdx.x - kEpiWarp0 * 32;   // 0 .. 255
                 for (int e0 = t; e0 < E4; e0 += kEpiWarps * 32 * kRedUnroll) {
                     float4 v[kRedUnroll][kMaxSplits];
 #pragma unroll
                     for (int u = 0; u < kRedUnroll; ++u) {
-                        const int e = e0 + u * kEpiWarps * 32;
+                        const int e4 = e0 + u * kEpiWarps * 32;
 #pragma unroll
                         for (int sidx = 0; sidx < kMaxSplits; ++sidx)
-                            if (sidx < p.S && e < E4) v[u][sidx] = __ldcg(base + (int64_t)sidx * E4 + e);
+                            if (sidx < p.S && e4 < E4) v[u][sidx] = __ldcg(base + (int64_t)sidx * E4 + e4);
                     }
 #pragma unroll
                     for (int u = 0; u < kRedUnroll; ++u) {
-                        const int e = e0 + u * kEpiWarps * 32;
-                        if (e >= E4) continue;
+                        const int e4 = e0 + u * kEpiWarps * 32;
+                        if (e4 >= E4) continue;
                         float4 sum = v[u][0];
 #pragma unroll
                         for (int sidx = 1; sidx < kMaxSplits; ++sidx) {
@@ -684,18 +702,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sum.w += v[u][sidx].w;
                             }
                         }
-                        const int col = (e * 4) / BM, r = e * 4 - col * BM;
+                        const int col = (e4 * 4) / BM, r = e4 * 4 - col * BM;
                         const int64_t n = (int64_t)tile * BM + r;
-                        if (col >= p.M || n >= p.N) continue;      // N % 16 == 0: all four in or out
+                        if (col >= m_real || n >= p.N) continue;   // N % 16 == 0: all four in or out
+                        const int64_t row = e * p.cap + col;
                         if (OUT_F32) {
-                            *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + (int64_t)col * p.ldc + n) = sum;
+                            *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + row * p.ldc + n) = sum;
                         } else {
                             const __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x, sum.y);
                             const __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z, sum.w);
                             uint2 o;
                             memcpy(&o.x, &lo, 4);
                             memcpy(&o.y, &hi, 4);
-                            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.C) + (int64_t)col * p.ldc + n) = o;
+                            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.C) + row * p.ldc + n) = o;
                         }
                     }
                 }
@@ -903,6 +922,17 @@ size_t round256(size_t v)
     return (v + 255) / 256 * 256;
 }
 
+// Split count of the masked layout, from the B300's 148 SMs rather than the
+// device's, so that the workspace size a caller queries and the launch agree.
+constexpr int kNominalSms = 148;
+int masked_splits(int32_t E, int64_t n_tiles, int64_t KB)
+{
+    int64_t S = kNominalSms / ((int64_t)E * n_tiles);
+    if (S > kMaxSplits) S = kMaxSplits;
+    if (S > KB) S = KB;
+    return S < 1 ? 1 : (int)S;
+}
+
 }  // namespace
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int)
@@ -917,6 +947,20 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts
         bytes += (size_t)tiles * smax * small_nt(M) * BM * 4;
     }
     return bytes;
+}
+
+size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K)
+{
+    const int64_t tiles = (N + BM - 1) / BM;
+    const int S = masked_splits(num_experts, tiles, K / BK);
+    size_t bytes = kWsHeaderBytes + round256((size_t)num_experts * tiles * 4);
+    if (S > 1) bytes += (size_t)num_experts * tiles * S * small_nt(cap) * BM * 4;
+    return bytes;
+}
+
+size_t masked_workspace_zeroed_bytes(int32_t num_experts, int64_t N)
+{
+    return kWsHeaderBytes + round256((size_t)num_experts * ((N + BM - 1) / BM) * 4);
 }
 
 size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t, int32_t num_experts)
@@ -972,30 +1016,33 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     p.K = a.K;
     p.KB = (int32_t)(a.K / BK);
     p.n_tiles = (int32_t)((a.N + BM - 1) / BM);
-    p.S = small_splits(a.N, a.K, num_sms);
+    const int32_t E = a.counts != nullptr ? a.num_experts : 1;
+    p.S = a.counts != nullptr ? masked_splits(E, p.n_tiles, p.KB) : small_splits(a.N, a.K, num_sms);
     p.C = a.C;
     p.ldc = a.ldc;
+    p.counts = a.counts;
+    p.cap = a.counts != nullptr ? a.cap : a.M;
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     p.status = reinterpret_cast<DeviceStatus *>(ws);
     p.tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
-    p.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + round256((size_t)p.n_tiles * 4));
+    p.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + round256((size_t)E * p.n_tiles * 4));
     CUtensorMap tmW, tmX, tmSA, tmSB;
-    if (!make_tensor_map_2d(&tmW, 1, false, a.B, a.K, a.N, a.K, BK, BM, true) ||
-        !make_tensor_map_2d(&tmX, 1, false, a.A, a.K, a.M, a.K, BK, NT, true) ||
+    if (!make_tensor_map_2d(&tmW, 1, false, a.B, a.K, (uint64_t)E * a.N, a.K, BK, BM, true) ||
+        !make_tensor_map_2d(&tmX, 1, false, a.A, a.K, (uint64_t)E * p.cap, a.K, BK, NT, true) ||
         !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, 1, false) ||
-        !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, p.KB, a.ldsb * 4, 4, 1, false))
+        !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, 1, false))
         return cudaErrorInvalidValue;
     auto kern = gemm_smallm_kernel<NT, STAGES, 8, OUT_F32>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
-    kern<<<p.n_tiles * p.S, kThreads, L::dyn_bytes, stream>>>(tmW, tmX, tmSA, tmSB, p);
+    kern<<<E * p.n_tiles * p.S, kThreads, L::dyn_bytes, stream>>>(tmW, tmX, tmSA, tmSB, p);
     return cudaGetLastError();
 }
 
 template <bool OUT_F32>
 cudaError_t launch_small_nt(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
-    switch (small_nt(a.M)) {
+    switch (small_nt(a.counts != nullptr ? a.cap : a.M)) {
     case 16: return launch_small<16, 8, OUT_F32>(a, stream, num_sms);
     case 32: return launch_small<32, 8, OUT_F32>(a, stream, num_sms);
     case 64: return launch_small<64, 8, OUT_F32>(a, stream, num_sms);
@@ -1024,6 +1071,11 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
         return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
     if (choose_bn(a, num_sms) == 128) return launch_bn<128, 6>(a, stream, num_sms);
     return launch_bn<256, 4>(a, stream, num_sms);
+}
+
+cudaError_t launch_masked(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
 }
 
 cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,

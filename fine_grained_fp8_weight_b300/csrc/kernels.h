@@ -35,6 +35,12 @@ struct GemmArgs {
     int32_t num_experts;
     void *workspace;
     size_t ws_bytes;
+    // masked grouped layout (decode MoE): when counts != nullptr, A and C hold
+    // num_experts slots of `cap` token rows (sa their scales, slot e at column
+    // e*cap), B num_experts weight matrices of N rows, sb num_experts scale
+    // blocks of K/128 rows
+    const int32_t *counts = nullptr;
+    int64_t cap = 0;
 };
 
 // Workspace layout: [0, 256) status word; then, for small M, the split-K
@@ -46,6 +52,10 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts
 // status word and the split-K arrival counters).
 size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
+// Masked grouped layout: scratch size, its zero-initialised prefix, launch.
+size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);
+size_t masked_workspace_zeroed_bytes(int32_t num_experts, int64_t N);
+cudaError_t launch_masked(const GemmArgs &a, cudaStream_t stream, int num_sms);
 cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,
                              cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(void *workspace, uint32_t budget_us, cudaStream_t stream);

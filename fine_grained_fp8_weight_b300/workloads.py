@@ -101,6 +101,17 @@ class Dgrad:
 
 
 @dataclass
+class Masked:
+    """Masked-layout grouped GEMM (decode MoE): A [E, cap, K] token slots of
+    which the first counts[e] rows are real, B [E, N, K]."""
+    name: str
+    A: np.ndarray                 # [E, cap, K], rows past the count are zero
+    B: np.ndarray                 # [E, N, K]
+    counts: np.ndarray            # [E] int32
+    out: str = "bf16"
+
+
+@dataclass
 class Workload:
     name: str
     gemms: list = field(default_factory=list)
@@ -198,3 +209,33 @@ def dgrad(seed: int = 5, T: int = 4096, N: int = 18432, K: int = 7168) -> Worklo
     dY = bf16_normal(rng, (T, N), 1.0, 0.001, 50.0)
     W = bf16_normal(rng, (N, K), 0.02)
     return Workload(f"dgrad_{T}x{K}x{N}", [Dgrad("dgrad", dY, W)])
+
+
+def masked_small(seed, counts, cap, N, K):
+    """Small masked-layout case for parity tests: slots [E, cap, K] N(0,1)
+    (rows past each count zero), B [E, N, K] N(0,0.02)."""
+    rng = np.random.default_rng(seed)
+    counts = np.asarray(counts, np.int32)
+    E = len(counts)
+    A = np.zeros((E, cap, K), np.uint16)
+    for e in range(E):
+        if counts[e]:
+            A[e, :counts[e]] = bf16_normal(rng, (int(counts[e]), K), 1.0, 0.001, 50.0)
+    B = np.stack([bf16_normal(rng, (N, K), 0.02) for _ in range(E)])
+    return Workload(f"masked_{E}x{cap}x{N}x{K}", [Masked("masked", A, B, counts)])
+
+
+def moe_decode(seed: int = 6, E: int = 32, cap: int = 256, tokens: int = 2048, N: int = 4096, K: int = 7168) -> Workload:
+    """Decode-time MoE in the masked layout: `tokens` routed tokens spread over
+    E experts by a Dirichlet(1) share and a multinomial draw, each expert's
+    count capped at its slot size `cap`; slots [E, cap, K] N(0,1) with 0.1%
+    outliers x50 (rows past the count zero), expert weights [E, N, K] N(0,0.02)."""
+    rng = np.random.default_rng(seed)
+    share = rng.dirichlet(np.ones(E))
+    counts = np.minimum(rng.multinomial(tokens, share), cap).astype(np.int32)
+    A = np.zeros((E, cap, K), np.uint16)
+    for e in range(E):
+        if counts[e]:
+            A[e, :counts[e]] = bf16_normal(rng, (int(counts[e]), K), 1.0, 0.001, 50.0)
+    B = np.stack([bf16_normal(rng, (N, K), 0.02) for _ in range(E)])
+    return Workload(f"moe_decode_{E}x{cap}x{N}x{K}", [Masked("masked", A, B, counts)])

@@ -234,6 +234,43 @@ fgf8_status fp8_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int6
                                          int64_t M_total, int64_t N, int64_t K,
                                          void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * fp8_masked_grouped_gemm_blockscaled -- the block-scaled GEMM for decode-time
+ * MoE in the masked layout: expert e owns a slot of `cap` token rows of A and
+ * of C and its own weight matrix B_e; only its first counts[e] tokens are real.
+ * At decode a few hundred tokens at most reach one expert, so the work is
+ * bound by reading the expert's weights ([kailasan] decode passage: small
+ * per-expert batches, memory access the bottleneck).  For m < counts[e]:
+ *   C[e][m][n] = sum_kb P_kb[m][n] * sa[e][kb][m] * sb[e][kb][n/128]
+ * with P_kb the 128-wide K partial as in fp8_gemm_blockscaled.  An expert with
+ * counts[e] == 0 reads none of its weights.
+ *
+ *   A  : E4M3 [E][cap][K] (row stride K), 16-byte aligned.  cap % 16 == 0,
+ *        16 <= cap <= 256.
+ *   sa : float [K/128][ldsa], ldsa >= E*cap, ldsa % 4 == 0: the scales of the
+ *        stacked slots, expert e's token m in column e*cap + m -- what
+ *        fp8_quant_act_1x128 writes for the [E*cap][K] buffer.
+ *   B  : E4M3 [E][N][K], 16-byte aligned.  N % 16 == 0, K % 128 == 0.
+ *   sb : float [E][K/128][ldsb], ldsb >= ceil(N/128), ldsb % 4 == 0.
+ *   counts : DEVICE int32 [E], 4-byte aligned, read by the kernel (no host
+ *        synchronisation); values are clamped to [0, cap].
+ *   C  : [E][cap][ldc] BF16 or FP32, ldc >= N, ldc * element size % 16 == 0;
+ *        rows m >= counts[e] are not written.
+ *   num_experts : 0 .. 65535 (0 is a no-op that reads no pointer).
+ *   workspace : at least fgf8_masked_gemm_workspace_bytes(E, cap, N, K) bytes,
+ *        256-byte aligned, zero-filled before its first use (status word and
+ *        one arrival counter per expert and 128 weight rows; the kernel leaves
+ *        them zero).  Calls sharing a workspace must not overlap on the GPU.
+ */
+fgf8_status fp8_masked_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa, const uint8_t *B,
+                                                const float *sb, int64_t ldsb, const int32_t *counts,
+                                                int32_t num_experts, int64_t cap, void *C, int64_t ldc,
+                                                fgf8_out_dtype cdt, int64_t N, int64_t K, void *workspace,
+                                                size_t ws_bytes, void *stream);
+
+/* Workspace bytes fp8_masked_grouped_gemm_blockscaled needs for these sizes. */
+size_t fgf8_masked_gemm_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);
+
 /* Workspace size (bytes) needed by the GEMM entry points for this shape. */
 size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 

@@ -203,7 +203,9 @@ def grouped_gemm_blockscaled(A, sa, B, sb, m_indices, rows=None):
 def masked_grouped_gemm_blockscaled(A, sa, B, sb, counts, rows_per_expert=None):
     """Masked-layout grouped reference (decode MoE): expert e owns a slot of
     `cap` token rows, of which the first counts[e] are real.
-    A [E, cap, K] codes, sa [E, K/128, lda_s]; B [E, N, K], sb [E, K/128, ldb_s].
+    A [E, cap, K] codes with sa [K/128, lda_s] the scales of the stacked slots
+    (expert e's token m in column e*cap + m, as a 1x128 quantization of the
+    [E*cap, K] buffer writes them); B [E, N, K], sb [E, K/128, ldb_s].
     Returns C, S of shape [E, cap, N]: for every expert the dense block-scaled
     GEMM of its real rows with its own weights; rows past the count are NaN
     (S = 0).  ``rows_per_expert``: optional list of row indices to evaluate
@@ -222,7 +224,8 @@ def masked_grouped_gemm_blockscaled(A, sa, B, sb, counts, rows_per_expert=None):
             rows = [r for r in rows_per_expert if r < c]
             if not rows:
                 continue
-        Ce, Se = gemm_blockscaled(A[e, :c], sa[e], B[e], sb[e], 0, rows=rows)
+        sa_e = np.ascontiguousarray(np.asarray(sa, np.float32)[:, e * cap:(e + 1) * cap])
+        Ce, Se = gemm_blockscaled(A[e, :c], sa_e, B[e], sb[e], 0, rows=rows)
         idx = rows if rows is not None else slice(0, c)
         C[e, idx] = Ce
         S[e, idx] = Se

@@ -264,3 +264,67 @@ def test_full_size_dgrad_sampled():
     rows = _sample_rows(g.dY.shape[0], 3, 15)
     Cr, S = oracle.gemm_blockscaled(qa, sa, rqT, rsT, rows=rows)
     assert_within_bound(bf16_out_to_f64(C)[rows], Cr, S, "dgrad")
+
+
+# --- masked-layout grouped GEMM (decode MoE): per-expert token slots + counts ---
+
+
+def _masked_inputs(w):
+    g = w.gemms[0]
+    E, cap, K = g.A.shape
+    qa, sa = oracle.quant_act_1x128(g.A.reshape(E * cap, K))          # stacked slots
+    qbs, sbs = zip(*[oracle.quant_w_128x128(g.B[e]) for e in range(E)])
+    return g, qa.reshape(E, cap, K), sa, np.stack(qbs), np.stack(sbs)
+
+
+def _run_masked(w, dt, rows=None, workspace=None):
+    g, qa, sa, qb, sb = _masked_inputs(w)
+    E, cap, K = qa.shape
+    N = qb.shape[1]
+    out = torch.full((E, cap, N), float("nan"), dtype=dt, device=DEV)
+    counts = torch.from_numpy(g.counts).to(DEV)
+    fg.fp8_masked_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), counts, out=out, workspace=workspace)
+    torch.cuda.synchronize()
+    Cr, S = oracle.masked_grouped_gemm_blockscaled(qa, sa, qb, sb, g.counts, rows_per_expert=rows)
+    Cg = out.float().cpu().numpy().astype(np.float64) if dt == torch.float32 else bf16_out_to_f64(out.reshape(E * cap, N)).reshape(E, cap, N)
+    return g, Cg, Cr, S
+
+
+# E x weight tiles below the SM count -> K split with the ticketed reduction;
+# 40 x 4 tiles -> one split, direct stores; token widths 16, 64, 256
+@pytest.mark.parametrize("counts,cap,N,K", [([64, 5, 0, 33], 64, 256, 512), ([16, 1], 16, 128, 256),
+                                            ([256, 0, 200, 17, 1, 128, 255, 64], 256, 512, 1024),
+                                            ([int(c) for c in np.random.default_rng(5).integers(0, 33, 40)], 32, 512, 512)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_masked_grouped(counts, cap, N, K, out):
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    w = wl.masked_small(len(counts) * 7 + cap + N, counts, cap, N, K)
+    g, Cg, Cr, S = _run_masked(w, dt)
+    for e, c in enumerate(g.counts):
+        if c:
+            assert_within_bound(Cg[e, :c], Cr[e, :c], S[e, :c], f"masked expert {e}")
+        assert np.all(np.isnan(Cg[e, c:])), f"rows past the count of expert {e} were written"
+
+
+def test_masked_grouped_repeated_calls_same_workspace():
+    w = wl.masked_small(3, [40, 0, 7, 64], 64, 256, 1024)
+    g, qa, sa, qb, sb = _masked_inputs(w)
+    ws = torch.zeros(fg.lib().fgf8_masked_gemm_workspace_bytes(4, 64, 256, 1024) + 4096, dtype=torch.uint8, device=DEV)
+    counts = torch.from_numpy(g.counts).to(DEV)
+    outs = [fg.fp8_masked_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), counts, workspace=ws)
+            for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        for e, c in enumerate(g.counts):
+            assert torch.equal(o[e, :c], outs[0][e, :c]), "split order must be deterministic"
+    assert fg.fgf8_read_status(ws) == (0, 0)
+    assert int(ws[256:256 + 4 * 2 * 4].view(torch.int32).abs().sum()) == 0, "arrival counters left non-zero"
+
+
+def test_full_size_moe_decode_sampled():
+    w = wl.moe_decode()
+    g, Cg, Cr, S = _run_masked(w, torch.bfloat16, rows=[0, 1, 63, 130, 255])
+    for e, c in enumerate(g.counts):
+        for r in (0, 1, 63, 130, 255):
+            if r < c:
+                assert_within_bound(Cg[e, r:r + 1], Cr[e, r:r + 1], S[e, r:r + 1], f"moe decode expert {e} row {r}")

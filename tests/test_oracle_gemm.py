@@ -178,8 +178,9 @@ def _masked_case(seed, E, cap, N, K, counts):
     bv, B = _int_codes(rng, (E, N, K))
     ja = rng.integers(-3, 4, size=(E, K // 128, cap))
     jb = rng.integers(-3, 4, size=(E, K // 128, (N + 127) // 128))
-    sa = np.zeros((E, K // 128, (cap + 3) // 4 * 4), np.float32)
-    sa[:, :, :cap] = np.exp2(ja)
+    sa = np.zeros((K // 128, E * cap + 4), np.float32)          # stacked slots, spare columns
+    for e in range(E):
+        sa[:, e * cap:(e + 1) * cap] = np.exp2(ja[e])
     sb = np.zeros((E, K // 128, ((N + 127) // 128 + 3) // 4 * 4), np.float32)
     sb[:, :, :jb.shape[2]] = np.exp2(jb)
     return av, A, bv, B, ja, jb, sa, sb
@@ -188,7 +189,7 @@ def _masked_case(seed, E, cap, N, K, counts):
 def test_masked_grouped_integer_experts():
     # exact: integer codes, power-of-two scales, sums far below 2^53
     E, cap, N, K = 3, 48, 144, 256
-    counts = np.array([48, 0, 17], np.int32)
+    counts = np.array([48, 0, 17], np.int32)      # cap 48: slots need not be powers of two
     av, A, bv, B, ja, jb, sa, sb = _masked_case(31, E, cap, N, K, counts)
     C, S = oracle.masked_grouped_gemm_blockscaled(A, sa, B, sb, counts)
     for e in range(E):
@@ -216,7 +217,7 @@ def test_masked_grouped_equals_contiguous_grouped():
         for r in range(pad):
             rows.append(A[e, r] if r < counts[e] else np.zeros(K, np.uint8))
             m_idx.append(e if r < counts[e] else -1)
-            sa_c.append(sa[e, :, r] if r < counts[e] else np.zeros(K // 128, np.float32))
+            sa_c.append(sa[:, e * cap + r] if r < counts[e] else np.zeros(K // 128, np.float32))
     Ac = np.stack(rows)
     sac = np.zeros((K // 128, (len(rows) + 3) // 4 * 4), np.float32)
     sac[:, :len(rows)] = np.stack(sa_c, axis=1)
