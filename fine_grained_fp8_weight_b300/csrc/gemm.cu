@@ -488,6 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c == 0) return;                      // idle expert: its weights are not even read
         m_real = c;
     }
+    // token columns actually computed: the real tokens rounded up to the MMA's
+    // N granularity (16); loads, MMAs and promotion stop there
+    const int32_t nt_run = m_real >= NT ? NT : (int32_t)((m_real + 15) / 16 * 16);
     const int32_t kb0 = (int32_t)((int64_t)split * p.KB / p.S);
     const int32_t kb1 = (int32_t)((int64_t)(split + 1) * p.KB / p.S);
     const int32_t ngroups = kb1 - kb0;
@@ -531,9 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + L::x_bytes));
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + nt_run * BK));
                 tma_load_2d(sm_w + s * L::w_bytes, &tmW, &full[s], (kb0 + g) * BK, (int32_t)(e * p.N) + tile * BM);
-                tma_load_2d(sm_x + s * L::x_bytes, &tmX, &full[s], (kb0 + g) * BK, (int32_t)(e * p.cap));
+                for (int32_t r = 0; r < nt_run; r += 16)   // 16-row boxes: whole 128B-swizzle atoms
+                    tma_load_2d(sm_x + s * L::x_bytes + r * BK, &tmX, &full[s], (kb0 + g) * BK,
+                                (int32_t)(e * p.cap) + r);
             }
         }
         __syncwarp();
@@ -555,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        const uint32_t idesc = idesc_e4m3_f32(BM, NT);
+        const uint32_t idesc = idesc_e4m3_f32(BM, (uint32_t)nt_run);
         bool ok = true;
         for (int32_t g = 0; g < ngroups; ++g) {
             const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
@@ -616,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
 #pragma unroll
             for (int c = 0; c < COLS; c += CH) {
+                if ((int32_t)(col0 + c) >= nt_run) break;      // no token columns left (warp-uniform)
                 uint32_t r[CH];
                 tmem_ld_sync<CH>(tmem_base + lane_addr + buf * NT + col0 + c, r);
 #pragma unroll
@@ -676,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // order, four outputs per float4, kRedUnroll of them in flight
                 __threadfence();
                 constexpr int kRedUnroll = 4;
-                constexpr int E4 = NT * BM / 4;                 // float4 per partial
+                constexpr int E4s = NT * BM / 4;                // float4 per partial (its stride)
+                const int E4 = nt_run * BM / 4;                 // the computed token columns
                 const float4 *base = reinterpret_cast<const float4 *>(p.partials + (int64_t)et * p.S * NT * BM);
                 const int t = (int)threadIdx.x - kEpiWarp0 * 32;   // 0 .. 255
                 for (int e0 = t; e0 < E4; e0 += kEpiWarps * 32 * kRedUnroll) {
@@ -686,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int e4 = e0 + u * kEpiWarps * 32;
 #pragma unroll
                         for (int sidx = 0; sidx < kMaxSplits; ++sidx)
-                            if (sidx < p.S && e4 < E4) v[u][sidx] = __ldcg(base + (int64_t)sidx * E4 + e4);
+                            if (sidx < p.S && e4 < E4) v[u][sidx] = __ldcg(base + (int64_t)sidx * E4s + e4);
                     }
 #pragma unroll
                     for (int u = 0; u < kRedUnroll; ++u) {
@@ -1028,7 +1035,7 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     p.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + round256((size_t)E * p.n_tiles * 4));
     CUtensorMap tmW, tmX, tmSA, tmSB;
     if (!make_tensor_map_2d(&tmW, 1, false, a.B, a.K, (uint64_t)E * a.N, a.K, BK, BM, true) ||
-        !make_tensor_map_2d(&tmX, 1, false, a.A, a.K, (uint64_t)E * p.cap, a.K, BK, NT, true) ||
+        !make_tensor_map_2d(&tmX, 1, false, a.A, a.K, (uint64_t)E * p.cap, a.K, BK, 16, true) ||
         !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, 1, false) ||
         !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, 1, false))
         return cudaErrorInvalidValue;
