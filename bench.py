@@ -43,10 +43,9 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
-    # captured on 0.3; 0.4 changed only the transposed quantizer (gemm.cu identical)
-    "fgf8 0.4 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_up.md
-        "prefill_pair_4096x18432x7168/up.gemm": 167115520 + 127643904,
-        "prefill_pair_4096x18432x7168/down.gemm": 627432192 + 52022784,
+    "fgf8 0.5 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_up.md
+        "prefill_pair_4096x18432x7168/up.gemm": 167170048 + 127274240,
+        "prefill_pair_4096x18432x7168/down.gemm": 627054848 + 51585280,
     },
 }
 

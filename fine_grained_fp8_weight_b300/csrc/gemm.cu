@@ -68,6 +68,9 @@ struct Params {
     int64_t b_rows_per_expert;          // N (grouped)
     int32_t sb_rows_per_expert;         // KB (grouped)
     DeviceStatus *status;
+    const float *sa;                    // scales, copied by the scale warp with cp.async
+    const float *sb;
+    int64_t ldsa, ldsb;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a)
@@ -79,7 +82,6 @@ template <int BN, int STAGES, int SC, bool ROW_SB>
 struct Layout {
     static constexpr size_t a_bytes = (size_t)BM * BK;
     static constexpr size_t b_bytes = (size_t)BN * BK;
-    static constexpr int sb_floats = ROW_SB ? BN : 4;        // floats copied per K group
     static constexpr int sb_slot = ROW_SB ? BN : 32;         // slot pitch: 128-byte aligned TMA targets
     static constexpr size_t off_a = 0;
     static constexpr size_t off_b = off_a + STAGES * a_bytes;
@@ -92,6 +94,12 @@ struct Layout {
     static constexpr size_t dyn_bytes = total + 1024;    // slack to align the base to 1024
     static constexpr uint32_t tmem_cols = 2 * BN;        // two partial buffers
 };
+
+// Wait until this thread's cp.async copies have landed (before a CTA exits).
+__device__ __forceinline__ void scale_copies_wait()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 __device__ __forceinline__ void tile_coords(int32_t tile, const Params &p, int32_t &mb, int32_t &nb)
 {
@@ -127,7 +135,6 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, float2 a, float
 template <int BN, int STAGES, int SC, bool ROW_SB, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                             const Params p)
 {
     using L = Layout<BN, STAGES, SC, ROW_SB>;
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < SC; ++i) {
-            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_full[i], 32);                 // one cp.async arrival per scale-warp lane
             mbar_init(&sc_empty[i], kEpiWarps);
         }
         for (int i = 0; i < 2; ++i) {
@@ -181,8 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            tma_prefetch_desc(&tmSA);
-            tma_prefetch_desc(&tmSB);
             uint32_t it = 0;
             bool ok = true;
             for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
@@ -213,38 +218,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kScaleWarp) {
-        // The scale vectors of each K group (512 bytes of sa, and 16 bytes of
-        // block sb or BN*4 bytes of per-row sb) stream through their own ring,
-        // so they run up to SC groups ahead, independent of the A/B stages.
-        if (elect_one()) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-                int32_t mb, nb;
-                tile_coords(tile, p, mb, nb);
-                const int32_t e = block_expert(p, mb);
-                if (e < 0) continue;
-                const int32_t s_row0 = e * p.sb_rows_per_expert;
-                const int32_t sb_x = ROW_SB ? nb * BN : ((nb * BN / 128) & ~3);
-                for (int32_t kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t j = it % SC, phj = (it / SC) & 1;
-                    if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
-                        record_timeout(p.status, kSiteProducerScale);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(BM * 4 + L::sb_floats * 4));
-                    tma_load_2d(sm_sa + j * BM, &tmSA, &sc_full[j], mb * BM, kb);
-                    tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], sb_x, s_row0 + kb);
+        // The scale vectors of each K group (128 floats of sa, and 4 floats of
+        // block sb or BN floats of per-row sb) are copied by the whole warp
+        // with 16-byte cp.async copies: generic-proxy writes that do not queue
+        // behind the operand tiles in the TMA unit.  Chunks past the end of a
+        // scale row are zero-filled without a read.
+        uint32_t it = 0;
+        bool ok = true;
+        for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            int32_t mb, nb;
+            tile_coords(tile, p, mb, nb);
+            const int32_t e = block_expert(p, mb);
+            if (e < 0) continue;
+            const int64_t s_row0 = (int64_t)e * p.sb_rows_per_expert;
+            const int64_t sa_x = (int64_t)mb * BM + 4 * lane;
+            for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t j = it % SC, phj = (it / SC) & 1;
+                if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+                    record_timeout(p.status, kSiteProducerScale);
+                    ok = false;
+                    break;
                 }
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                const uint32_t first = it > (uint32_t)SC ? it - SC : 0;
-                for (uint32_t i = first; i <= it; ++i)
-                    mbar_wait(&sc_full[i % SC], (i / SC) & 1, nullptr, 20u * 1000u * 1000u);
+                cp_async_16_zfill(sm_sa + j * BM + 4 * lane, p.sa + (int64_t)kb * p.ldsa + (sa_x < p.ldsa ? sa_x : 0),
+                                  sa_x < p.ldsa ? 16u : 0u);
+                const float *sb_row = p.sb + (s_row0 + kb) * p.ldsb;
+                if constexpr (ROW_SB) {
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) {
+                        const int64_t x = (int64_t)nb * BN + h * 128 + 4 * lane;
+                        cp_async_16_zfill(sm_sb + j * L::sb_slot + h * 128 + 4 * lane, sb_row + (x < p.ldsb ? x : 0),
+                                          x < p.ldsb ? 16u : 0u);
+                    }
+                } else if (lane == 0) {
+                    cp_async_16_zfill(sm_sb + j * L::sb_slot, sb_row + ((nb * BN / 128) & ~3), 16u);
+                }
+                cp_async_arrive_noinc(&sc_full[j]);
             }
         }
+        if (!ok) *abort_flag = 1;
+        scale_copies_wait();
         __syncwarp();
     } else if (warp == kMmaWarp) {
         const uint32_t idesc = idesc_e4m3_f32(BM, BN);
@@ -354,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                fence_proxy_async_smem();     // scale slot j is refilled by TMA once released
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -865,19 +876,15 @@ template <int BN, int STAGES, int SC, bool ROW_SB, bool OUT_F32>
 cudaError_t launch_variant(const GemmArgs &a, const Params &p, int grid, cudaStream_t stream)
 {
     using L = Layout<BN, STAGES, SC, ROW_SB>;
-    CUtensorMap tmA, tmB, tmSA, tmSB;
-    const int64_t KB = a.K / BK;
+    CUtensorMap tmA, tmB;
     const int64_t b_rows = a.m_indices ? (int64_t)a.num_experts * a.N : a.N;
-    const int64_t sb_rows = a.m_indices ? (int64_t)a.num_experts * KB : KB;
     if (!make_tensor_map_2d(&tmA, 1, false, a.A, a.K, a.M, a.K, BK, BM, true) ||
-        !make_tensor_map_2d(&tmB, 1, false, a.B, a.K, b_rows, a.K, BK, BN, true) ||
-        !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, KB, a.ldsa * 4, BM, 1, false) ||
-        !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, sb_rows, a.ldsb * 4, L::sb_floats, 1, false))
+        !make_tensor_map_2d(&tmB, 1, false, a.B, a.K, b_rows, a.K, BK, BN, true))
         return cudaErrorInvalidValue;
     auto kern = gemm_blockscaled_kernel<BN, STAGES, SC, ROW_SB, OUT_F32>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, L::dyn_bytes, stream>>>(tmA, tmB, tmSA, tmSB, p);
+    kern<<<grid, kThreads, L::dyn_bytes, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 
@@ -997,6 +1004,10 @@ Params make_params(const GemmArgs &a)
     p.b_rows_per_expert = a.m_indices ? a.N : 0;
     p.sb_rows_per_expert = a.m_indices ? p.KB : 0;
     p.status = reinterpret_cast<DeviceStatus *>(a.workspace);
+    p.sa = a.sa;
+    p.sb = a.sb;
+    p.ldsa = a.ldsa;
+    p.ldsb = a.ldsb;
     return p;
 }
 

@@ -113,6 +113,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     return false;
 }
 
+// 16-byte global -> shared copy in the generic proxy (cp.async); with
+// `bytes` == 0 nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async_16_zfill(void *smem_dst, const void *gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem_dst)), "l"(gsrc), "r"(bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (the arrival is not counted in advance: the barrier's count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // ----------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
