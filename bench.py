@@ -184,6 +184,22 @@ def gemm_bytes(g):
     raise TypeError(g)
 
 
+def max_over_ranks(ms_total, dist=None, device=None):
+    """The job's time: the slowest rank's (replicas run the same step on their
+    own data; `value` is all ranks' work over this time)."""
+    if dist is None:
+        return ms_total
+    import torch
+    t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step, world, ms_step):
+    """Whole-job throughput: every rank's FLOPs of one step over the step time."""
+    return flops_per_rank_step * world / (ms_step * 1e-3) / 1e12
+
+
 class DevicePath:
     """The step on device buffers: every op is one C-ABI call on one stream."""
 
@@ -357,11 +373,7 @@ def run_device(args, rank, world, local_rank):
     t1.record()
     barrier()
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     ms_step = ms_total / args.steps
 
     # Per-kernel device time: each op captured alone and replayed, one event
@@ -401,7 +413,7 @@ def run_device(args, rank, world, local_rank):
         per_op[name] = entry
     n_ops = len(path.ops)
 
-    value = path.gemm_flops * world / (ms_step * 1e-3) / 1e12
+    value = job_tflops(path.gemm_flops, world, ms_step)
     # roofline of the dominant kernel: the GEMM launch that takes longest
     gemm_ops = [(per_op[name]["ms"], name, w) for kind, name, _, w in path.ops if kind == "gemm"]
     dom_ms, dom_name, dom_flops = max(gemm_ops)
