@@ -203,7 +203,7 @@ def job_tflops(flops_per_rank_step, world, ms_step):
 class DevicePath:
     """The step on device buffers: every op is one C-ABI call on one stream."""
 
-    def __init__(self, work, dev):
+    def __init__(self, work, dev, fused_a=False):
         import torch
         import fine_grained_fp8_weight_b300 as fg
         from fine_grained_fp8_weight_b300 import workloads as wl
@@ -223,6 +223,16 @@ class DevicePath:
                 C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                 self.outputs.append(C)
                 qbytes = lambda r, c, sc: r * c * 3 + sc * 4
+                if fused_a and M <= 64:
+                    # tokens quantized inside the GEMM: no activation-quantize launch
+                    self.ops.append(("quant", f"{g.name}.quant_w_128x128",
+                                     lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128(B)),
+                                     qbytes(N, K, (N // 128 + 1) * K // 128)))
+                    self.ops.append(("gemm", f"{g.name}.gemm",
+                                     lambda A=A, st=st, C=C: fg.fp8_gemm_bf16a_blockscaled(A, st["b"][0], st["b"][1],
+                                                                                          out=C),
+                                     gemm_flops(g)))
+                    continue
                 self.ops.append(("quant", f"{g.name}.quant_act_1x128",
                                  lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)),
                                  qbytes(M, K, M * K // 128)))
@@ -334,7 +344,7 @@ def run_device(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     work = make_workload(args.workload)
-    path = DevicePath(work, dev)
+    path = DevicePath(work, dev, fused_a=args.fused_a)
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
 
@@ -615,6 +625,8 @@ def main():
     ap.add_argument("--profile-gemm", action="store_true")
     ap.add_argument("--gemm-index", type=int, default=0)
     ap.add_argument("--profile-op", default=None, help="run one op of the workload repeatedly (for ncu)")
+    ap.add_argument("--fused-a", action="store_true",
+                    help="GEMMs with at most 64 tokens quantize their BF16 tokens inside the GEMM")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -42,7 +42,7 @@ STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED
 EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
             "fp8_quant_w_128x128_grouped", "fp8_quant_w_128x128_t",
             "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm_blockscaled",
-            "fp8_masked_grouped_gemm_blockscaled", "fgf8_gemm_workspace_bytes", "fgf8_masked_gemm_workspace_bytes",
+            "fp8_masked_grouped_gemm_blockscaled", "fp8_gemm_bf16a_blockscaled", "fgf8_gemm_workspace_bytes", "fgf8_masked_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div"]
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_masked_grouped_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, P, I32, I64, P, I64, ctypes.c_int,
                                                           I64, I64, P, SZ, P]
         L.fgf8_masked_gemm_workspace_bytes.argtypes = [I32, I64, I64, I64]
+        L.fp8_gemm_bf16a_blockscaled.argtypes = [P, I64, P, P, I64, P, I64, ctypes.c_int, I64, I64, I64, P, SZ, P]
         L.fgf8_masked_gemm_workspace_bytes.restype = SZ
         L.fgf8_read_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
@@ -208,6 +209,23 @@ def fp8_gemm_blockscaled(A, sa, B, sb, bkind: int = BSCALE_BLOCK128, out_dtype=t
                                     _ptr(out), out.stride(0), cdt, M, N, K, _ptr(ws), ws.numel(),
                                     _stream(A.device))
     _check(st, "fp8_gemm_blockscaled")
+    return out
+
+
+def fp8_gemm_bf16a_blockscaled(x, B, sb, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None):
+    """C = quant_1x128(x) * B_hat^T with x: BF16 [M, K] (M <= 64) quantized inside the GEMM."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    cdt = OUT_FP32 if out.dtype == torch.float32 else OUT_BF16
+    need = lib().fgf8_gemm_workspace_bytes(M, N, K, 1)
+    ws = workspace if workspace is not None else workspace_for(x.device, need)
+    st = lib().fp8_gemm_bf16a_blockscaled(_ptr(x), x.stride(0), _ptr(B), _ptr(sb), sb.stride(0), _ptr(out),
+                                          out.stride(0), cdt, M, N, K, _ptr(ws), ws.numel(), _stream(x.device))
+    _check(st, "fp8_gemm_bf16a_blockscaled")
     return out
 
 

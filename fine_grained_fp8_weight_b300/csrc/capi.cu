@@ -208,6 +208,32 @@ fgf8_status fp8_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int6
     return from_cuda(fgf8::launch_gemm(a, static_cast<cudaStream_t>(stream), num_sms));
 }
 
+fgf8_status fp8_gemm_bf16a_blockscaled(const void *x, int64_t ldx, const uint8_t *B, const float *sb, int64_t ldsb,
+                                       void *C, int64_t ldc, fgf8_out_dtype cdt, int64_t M, int64_t N, int64_t K,
+                                       void *workspace, size_t ws_bytes, void *stream)
+{
+    if (M == 0 || N == 0) return FGF8_OK;                // empty output: nothing to read or write
+    if (!x || !B || !sb || !C || !workspace) return FGF8_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 1) return FGF8_ERR_INVALID_ARG;
+    if (cdt != FGF8_OUT_BF16 && cdt != FGF8_OUT_FP32) return FGF8_ERR_INVALID_ARG;
+    if (M > 64 || K % 128 != 0 || N % 16 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (N > INT32_MAX / 2 || K > INT32_MAX / 2) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (ldx < K || ldsb < (N + 127) / 128 || ldsb % 4 != 0 || ldc < N) return FGF8_ERR_INVALID_ARG;
+    const int64_t esz = cdt == FGF8_OUT_BF16 ? 2 : 4;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(B, 16) || !aligned(sb, 16) || !aligned(C, 16) ||
+        (ldc * esz) % 16 != 0 || !aligned(workspace, 256))
+        return FGF8_ERR_MISALIGNED;
+    if (ws_bytes < fgf8::gemm_workspace_bytes(M, N, K, 1, 0)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
+    int num_sms = 0;
+    fgf8_status st = current_device(&num_sms);
+    if (st != FGF8_OK) return st;
+    fgf8::GemmArgs a{nullptr, nullptr, 0, B, sb, ldsb, 0, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M, N, K,
+                     nullptr, 1, workspace, ws_bytes};
+    a.xbf16 = x;
+    a.ldx = ldx;
+    return from_cuda(fgf8::launch_bf16a(a, static_cast<cudaStream_t>(stream), num_sms));
+}
+
 size_t fgf8_masked_gemm_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K)
 {
     if (num_experts < 1 || cap < 1 || N < 1 || K < 128) return fgf8::kWsHeaderBytes;

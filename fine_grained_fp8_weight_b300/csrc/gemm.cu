@@ -25,6 +25,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "e4m3_rule.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -54,6 +55,7 @@ enum : int32_t {
     kSiteEpiScale = 5,
     kSiteEpiTmemFull = 6,
     kSiteProbe = 7,
+    kSiteQuantFull = 8,
     kSiteSelftest = 99
 };
 
@@ -436,35 +438,43 @@ struct SmallParams {
     // counts == nullptr, cap == M.
     const int32_t *counts;
     int64_t cap;
+    const float *sb;          // QX: weight block scales read directly
+    int64_t ldsb;
 };
 
-template <int NT, int STAGES, int SC>
+template <int NT, int STAGES, int SC, bool QX = false>
 struct SmallLayout {
     static constexpr size_t w_bytes = (size_t)BM * BK;        // 16 KB of weights
-    static constexpr size_t x_bytes = (size_t)NT * BK;        // tokens
+    static constexpr size_t x_bytes = (size_t)NT * BK;        // tokens, E4M3 (swizzled, read by the MMA)
+    static constexpr size_t xb_bytes = QX ? (size_t)NT * BK * 2 : 0;   // tokens as BF16 (quantized in the kernel)
     static constexpr size_t off_w = 0;
     static constexpr size_t off_x = off_w + STAGES * w_bytes;
+    static constexpr size_t off_xb = align_up(off_x + STAGES * x_bytes, 1024);
     static constexpr int sa_slot = NT < 32 ? 32 : NT;          // floats; 128-byte aligned TMA targets
-    static constexpr size_t off_sa = align_up(off_x + STAGES * x_bytes, 1024);
+    static constexpr size_t off_sa = align_up(off_xb + STAGES * xb_bytes, 1024);
     static constexpr size_t off_sb = off_sa + (size_t)SC * sa_slot * 4;
     static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * 32 * 4, 16);
     // as many TMEM partial buffers as fit (up to 8): the MMA can run ahead of
     // the promotion by that many K groups
     static constexpr int nbuf = (512 / NT) < 8 ? (512 / NT) : 8;
-    static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1;
+    static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1 + (QX ? STAGES : 0);
     static constexpr size_t off_misc = off_bar + (size_t)num_bars * 8;
     static constexpr size_t total = off_misc + 16;
     static constexpr size_t dyn_bytes = total + 1024;
     static constexpr uint32_t tmem_cols = nbuf * NT < 32 ? 32 : nbuf * NT;   // power of two
 };
 
-template <int NT, int STAGES, int SC, bool OUT_F32>
+// QX: the token operand arrives as BF16 and is quantized 1x128 inside the
+// kernel (no E4M3 round trip through HBM): warps 2 and 3 turn each K group's
+// BF16 token tile into the swizzled E4M3 tile the MMA reads and its scales,
+// by the same rule and code as the quantization kernels (e4m3_rule.cuh).
+template <int NT, int STAGES, int SC, bool OUT_F32, bool QX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_smallm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                        const SmallParams p)
 {
-    using L = SmallLayout<NT, STAGES, SC>;
+    using L = SmallLayout<NT, STAGES, SC, QX>;
     constexpr int COLS = NT / 2;                 // token columns per promotion warp
     constexpr int CH = COLS < 32 ? COLS : 32;    // columns per TMEM load
     extern __shared__ uint8_t smem_raw[];
@@ -481,6 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tm_full = bars + 2 * STAGES + 2 * SC;
     uint64_t *tm_empty = tm_full + L::nbuf;
     uint64_t *drain = tm_full + 2 * L::nbuf;
+    uint64_t *qfull = drain + 1;                 // QX: stage s quantized (after full[s])
+    uint8_t *sm_xb = smem + L::off_xb;
     uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::off_misc + 4);   // [0] abort, [1] last
 
@@ -512,9 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < SC; ++i) {
-            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_full[i], QX ? 2 : 1);        // QX: one arrival per quantizer warp
             mbar_init(&sc_empty[i], kEpiWarps);
         }
+        if (QX)
+            for (int i = 0; i < STAGES; ++i) mbar_init(&qfull[i], 2);
         for (int i = 0; i < L::nbuf; ++i) {
             mbar_init(&tm_full[i], 1);
             mbar_init(&tm_empty[i], kEpiWarps);
@@ -545,15 +559,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + nt_run * BK));
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + nt_run * BK * (QX ? 2 : 1)));
                 tma_load_2d(sm_w + s * L::w_bytes, &tmW, &full[s], (kb0 + g) * BK, (int32_t)(e * p.N) + tile * BM);
-                for (int32_t r = 0; r < nt_run; r += 16)   // 16-row boxes: whole 128B-swizzle atoms
-                    tma_load_2d(sm_x + s * L::x_bytes + r * BK, &tmX, &full[s], (kb0 + g) * BK,
-                                (int32_t)(e * p.cap) + r);
+                for (int32_t r = 0; r < nt_run; r += 16) {  // 16-row boxes: whole 128B-swizzle atoms
+                    if (QX)
+                        tma_load_2d(sm_xb + s * L::xb_bytes + r * BK * 2, &tmX, &full[s], (kb0 + g) * BK,
+                                    (int32_t)(e * p.cap) + r);
+                    else
+                        tma_load_2d(sm_x + s * L::x_bytes + r * BK, &tmX, &full[s], (kb0 + g) * BK,
+                                    (int32_t)(e * p.cap) + r);
+                }
             }
         }
         __syncwarp();
-    } else if (warp == kScaleWarp) {
+    } else if (QX && (warp == kScaleWarp || warp == kScaleWarp + 1)) {
+        // Quantize each K group's token tile: a warp takes two token rows per
+        // pass (16 lanes x 8 values each), amax over the row by shuffles, the
+        // codes into the 128B-swizzled E4M3 tile (16-byte chunk c of row r at
+        // chunk c ^ (r & 7) of its 1024-byte atom), the scales into the ring.
+        const int wq = (int)warp - kScaleWarp;
+        const int c16 = (int)(lane & 15);
+        bool ok = true;
+        for (int32_t g = 0; g < ngroups; ++g) {
+            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+            const uint32_t j = g % SC, phj = (g / SC) & 1;
+            if (!mbar_wait(&full[s], ph, abort_flag)) {
+                record_timeout(p.status, kSiteQuantFull);
+                ok = false;
+                break;
+            }
+            if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+                record_timeout(p.status, kSiteProducerScale);
+                ok = false;
+                break;
+            }
+            const uint8_t *xb = sm_xb + s * L::xb_bytes;
+            uint8_t *xq = sm_x + s * L::x_bytes;
+            for (int32_t r0 = 0; r0 < nt_run; r0 += 4) {
+                const int r = r0 + 2 * wq + (int)(lane >> 4);
+                float f[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xb + r * (BK * 2) + c16 * 16), f);
+                float a = amax8(f);
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                const float sc = __fdiv_rn(a, kE4M3Max);
+                const uint2 c = encode8(f, make_divisor(sc));
+                uint8_t *row = xq + (r >> 3) * 1024 + (r & 7) * 128;
+                *reinterpret_cast<uint2 *>(row + (((c16 >> 1) ^ (r & 7)) * 16) + (c16 & 1) * 8) = c;
+                if (c16 == 0) sm_sa[j * L::sa_slot + r] = sc;
+            }
+            if (wq == 0 && lane == 0)
+                sm_sb[j * 32 + (tile & 3)] = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + g) * p.ldsb + tile);
+            fence_proxy_async_smem();     // E4M3 tile -> the MMA; BF16 stage -> its next TMA refill
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&qfull[s]);
+                mbar_arrive(&sc_full[j]);
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (!QX && warp == kScaleWarp) {
         if (elect_one()) {
             tma_prefetch_desc(&tmSA);
             tma_prefetch_desc(&tmSB);
@@ -581,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            if (!mbar_wait(&full[s], ph, abort_flag)) {
+            if (!mbar_wait(QX ? &qfull[s] : &full[s], ph, abort_flag)) {
                 record_timeout(p.status, kSiteMmaFull);
                 ok = false;
                 break;
@@ -896,7 +961,9 @@ bool make_tensor_map_2d(void *map, int dtype_bytes, bool is_float, const void *b
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const CUtensorMapDataType dt =
-        dtype_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : (is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32);
+        dtype_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+        : dtype_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+        : (is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32);
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {row_stride_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
@@ -1024,10 +1091,10 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
                      : launch_variant<BN, STAGES, 12, false, false>(a, p, grid, stream);
 }
 
-template <int NT, int STAGES, bool OUT_F32>
+template <int NT, int STAGES, bool OUT_F32, bool QX = false>
 cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
-    using L = SmallLayout<NT, STAGES, 8>;
+    using L = SmallLayout<NT, STAGES, 8, QX>;
     SmallParams p{};
     p.M = a.M;
     p.N = a.N;
@@ -1040,17 +1107,27 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     p.ldc = a.ldc;
     p.counts = a.counts;
     p.cap = a.counts != nullptr ? a.cap : a.M;
+    p.sb = a.sb;
+    p.ldsb = a.ldsb;
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     p.status = reinterpret_cast<DeviceStatus *>(ws);
     p.tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
     p.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + round256((size_t)E * p.n_tiles * 4));
     CUtensorMap tmW, tmX, tmSA, tmSB;
-    if (!make_tensor_map_2d(&tmW, 1, false, a.B, a.K, (uint64_t)E * a.N, a.K, BK, BM, true) ||
-        !make_tensor_map_2d(&tmX, 1, false, a.A, a.K, (uint64_t)E * p.cap, a.K, BK, 16, true) ||
-        !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, 1, false) ||
-        !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, 1, false))
+    memset(&tmSA, 0, sizeof(tmSA));
+    memset(&tmSB, 0, sizeof(tmSB));
+    if (!make_tensor_map_2d(&tmW, 1, false, a.B, a.K, (uint64_t)E * a.N, a.K, BK, BM, true))
         return cudaErrorInvalidValue;
-    auto kern = gemm_smallm_kernel<NT, STAGES, 8, OUT_F32>;
+    if (QX) {
+        // BF16 tokens, plain row-major 16 x 128 boxes (the kernel quantizes them)
+        if (!make_tensor_map_2d(&tmX, 2, false, a.xbf16, a.K, (uint64_t)E * p.cap, a.ldx * 2, BK, 16, false))
+            return cudaErrorInvalidValue;
+    } else if (!make_tensor_map_2d(&tmX, 1, false, a.A, a.K, (uint64_t)E * p.cap, a.K, BK, 16, true) ||
+               !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, 1, false) ||
+               !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, 1, false)) {
+        return cudaErrorInvalidValue;
+    }
+    auto kern = gemm_smallm_kernel<NT, STAGES, 8, OUT_F32, QX>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
     kern<<<E * p.n_tiles * p.S, kThreads, L::dyn_bytes, stream>>>(tmW, tmX, tmSA, tmSB, p);
@@ -1094,6 +1171,24 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
 cudaError_t launch_masked(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
     return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
+}
+
+namespace {
+template <bool OUT_F32>
+cudaError_t launch_small_qx(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    // stages so that the BF16 token staging fits next to the E4M3 tiles
+    switch (small_nt(a.M)) {
+    case 16: return launch_small<16, 8, OUT_F32, true>(a, stream, num_sms);
+    case 32: return launch_small<32, 6, OUT_F32, true>(a, stream, num_sms);
+    default: return launch_small<64, 5, OUT_F32, true>(a, stream, num_sms);
+    }
+}
+}  // namespace
+
+cudaError_t launch_bf16a(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    return a.out_f32 ? launch_small_qx<true>(a, stream, num_sms) : launch_small_qx<false>(a, stream, num_sms);
 }
 
 cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,

@@ -210,6 +210,26 @@ fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int6
                                          int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
+ * fp8_gemm_bf16a_blockscaled -- the block-scaled GEMM with its token operand
+ * given as BF16 and quantized 1x128 inside the GEMM, for decode-sized M:
+ * the E4M3 copy of the tokens never goes through HBM ([why-be]
+ * FP8-cast-with-TMA passage: the quantization round trip through memory, and
+ * the wish to fuse the cast into the load).  The codes and scales are those
+ * of fp8_quant_act_1x128 (same rule, same arithmetic), so the result equals
+ * fp8_quant_act_1x128 followed by fp8_gemm_blockscaled bit for bit.
+ *
+ *   x  : BF16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.  1 <= M <= 64.
+ *   B  : E4M3 [N][K] with 128x128 block scales sb [K/128][ldsb] as in
+ *        fp8_gemm_blockscaled (BLOCK128 kind).  N % 16 == 0, K % 128 == 0.
+ *   C  : [M][ldc] BF16 or FP32, as in fp8_gemm_blockscaled.
+ *   workspace : at least fgf8_gemm_workspace_bytes(M, N, K, 1) bytes, as in
+ *        fp8_gemm_blockscaled.  M == 0 or N == 0 is a no-op.
+ */
+fgf8_status fp8_gemm_bf16a_blockscaled(const void *x, int64_t ldx, const uint8_t *B, const float *sb, int64_t ldsb,
+                                       void *C, int64_t ldc, fgf8_out_dtype cdt, int64_t M, int64_t N, int64_t K,
+                                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * fp8_grouped_gemm_blockscaled -- MoE expert GEMM in the contiguous layout:
  * the rows of A are grouped by expert, each group padded to a multiple of 128
  * rows, and row m uses expert e = m_indices[m] ([dssusan] scheme applied per

@@ -328,3 +328,47 @@ def test_full_size_moe_decode_sampled():
         for r in (0, 1, 63, 130, 255):
             if r < c:
                 assert_within_bound(Cg[e, r:r + 1], Cr[e, r:r + 1], S[e, r:r + 1], f"moe decode expert {e} row {r}")
+
+
+# --- token operand given as BF16, quantized inside the GEMM (decode M <= 64) ---
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 7168), (5, 144, 2048), (33, 512, 1024), (64, 7168, 2048),
+                                   (64, 256, 128), (1, 16, 256)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_bf16a_equals_quantize_then_gemm(M, N, K, out):
+    # same rule and arithmetic as the quantization kernel: the fused GEMM must
+    # equal quantize + GEMM bit for bit, and the oracle within the bound
+    rng = np.random.default_rng(M * 11 + N + K)
+    X = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    W = wl.bf16_normal(rng, (N, K), 0.02)
+    qb, sb = fg.fp8_quant_w_128x128(dev_bf16(W))
+    x = dev_bf16(X)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    fused = fg.fp8_gemm_bf16a_blockscaled(x, qb, sb, out_dtype=dt)
+    qa, sa, _, _ = fg.fp8_quant_act_1x128(x)
+    twostep = fg.fp8_gemm_blockscaled(qa, sa, qb, sb, out_dtype=dt)
+    torch.cuda.synchronize()
+    iv = torch.int16 if dt == torch.bfloat16 else torch.int32
+    assert torch.equal(fused.view(iv), twostep.view(iv)), "fused quantization differs from the two-step path"
+    rqa, rsa = oracle.quant_act_1x128(X)
+    rqb, rsb = oracle.quant_w_128x128(W)
+    rows = _sample_rows(M, 16, M)
+    Cr, S = oracle.gemm_blockscaled(rqa, rsa, rqb, rsb, rows=rows)
+    Cg = bf16_out_to_f64(fused) if dt == torch.bfloat16 else fused.cpu().numpy().astype(np.float64)
+    assert_within_bound(Cg[rows], Cr, S, f"bf16a {M}x{N}x{K}")
+
+
+def test_bf16a_row_stride_and_rejects_large_m():
+    rng = np.random.default_rng(8)
+    X = wl.bf16_normal(rng, (32, 1024))
+    W = wl.bf16_normal(rng, (256, 512), 0.02)
+    big = dev_bf16(X)[:, :512]                       # ldx = 1024 > K = 512
+    qb, sb = fg.fp8_quant_w_128x128(dev_bf16(W))
+    fused = fg.fp8_gemm_bf16a_blockscaled(big, qb, sb)
+    qa, sa, _, _ = fg.fp8_quant_act_1x128(big.contiguous())
+    twostep = fg.fp8_gemm_blockscaled(qa, sa, qb, sb)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), twostep.view(torch.int16))
+    with pytest.raises(fg.FGF8Error, match="UNSUPPORTED_SHAPE"):
+        fg.fp8_gemm_bf16a_blockscaled(dev_bf16(wl.bf16_normal(rng, (65, 512))), qb, sb)
