@@ -7,16 +7,26 @@
 // must leave the tensor cores before it can be scaled; "kailasan.com
 // recruit post 147436" (hardware-suggestion passage) has the partial results
 // copied out at each interval, multiplied by the scaling factors and added
-// into FP32.  Here that interval is one 128-wide K group:
-//   - warp 0 (one lane) streams A/B tiles and the scale vectors with TMA into
-//     a ring of shared-memory stages;
+// into FP32.  Here that interval is one 128-wide K group.
+//
+// gemm_blockscaled_kernel (128 x 256 or 128 x 128 output tiles, persistent,
+// dense and grouped layouts):
+//   - warp 0 (one lane) streams the A/B tiles with TMA into a ring of
+//     shared-memory stages;
+//   - warp 2 copies each K group's scale vectors (sa, and block or per-row
+//     sb) into a separate ring with cp.async, running up to SC groups ahead;
 //   - warp 1 (one lane) issues 4 tcgen05.mma (K = 32 each) per K group into a
 //     fresh FP32 partial in tensor memory, alternating between two TMEM
 //     buffers so that the next group's MMAs run while this one is promoted;
-//   - warps 4..7 (the promotion warpgroup) read each partial with tcgen05.ld
-//     (one TMEM lane = one output row per thread), multiply by sa*sb and add
-//     into FP32 registers, then write the finished tile (BF16 or FP32).
-// The kernel is persistent: each CTA walks a static list of output tiles.
+//   - warps 4..11 (two promotion warpgroups, one TMEM lane = one output row
+//     per thread, half of the tile's columns each) read each partial with
+//     tcgen05.ld, multiply by sa*sb and add into FP32 registers, then write
+//     the finished tile (BF16 or FP32).
+// gemm_smallm_kernel (decode, M <= 256 tokens): the weight tile takes the
+// MMA's M side and the tokens its N side, K is split over CTAs with an
+// in-order reduction; the same kernel serves the masked grouped layout
+// (per-expert token slots with device-side counts) and, for M <= 64, the
+// variant that quantizes BF16 tokens inside the kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -84,7 +94,7 @@ template <int BN, int STAGES, int SC, bool ROW_SB>
 struct Layout {
     static constexpr size_t a_bytes = (size_t)BM * BK;
     static constexpr size_t b_bytes = (size_t)BN * BK;
-    static constexpr int sb_slot = ROW_SB ? BN : 32;         // slot pitch: 128-byte aligned TMA targets
+    static constexpr int sb_slot = ROW_SB ? BN : 32;         // slot pitch in floats (128-byte aligned slots)
     static constexpr size_t off_a = 0;
     static constexpr size_t off_b = off_a + STAGES * a_bytes;
     static constexpr size_t off_sa = off_b + STAGES * b_bytes;
