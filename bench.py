@@ -43,7 +43,9 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
-    "fgf8 0.5 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_up.md
+    # captured on 0.5; 0.6 changed only the E4M3 encode step (quantizers and the in-GEMM token
+    # quantizer), not gemm_blockscaled_kernel
+    "fgf8 0.6 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_up.md
         "prefill_pair_4096x18432x7168/up.gemm": 167170048 + 127274240,
         "prefill_pair_4096x18432x7168/down.gemm": 627054848 + 51585280,
     },

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kBlockThreads)
 // sub-block, and a warp (8 column octets x 4 row octets) writes 8 rows of W^T
 // x 32 contiguous bytes per store.
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBlockThreads)
+__global__ void __launch_bounds__(kBlockThreads, 3)
     quant_w_block_t_kernel(const __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
                            uint8_t *__restrict__ qT, float *__restrict__ sT, int64_t ldsT,
                            uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds)
