@@ -42,8 +42,10 @@ STATUS_NAMES = {0: "FGF8_OK", 1: "FGF8_ERR_INVALID_ARG", 2: "FGF8_ERR_MISALIGNED
 EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_quant_w_128x128",
             "fp8_quant_w_128x128_grouped", "fp8_quant_w_128x128_t",
             "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm_blockscaled",
-            "fp8_masked_grouped_gemm_blockscaled", "fp8_gemm_bf16a_blockscaled", "fgf8_gemm_workspace_bytes", "fgf8_masked_gemm_workspace_bytes",
-            "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div"]
+            "fp8_masked_grouped_gemm_blockscaled", "fp8_gemm_bf16a_blockscaled", "fgf8_gemm_workspace_bytes", "fgf8_gemm_workspace_min_bytes",
+            "fgf8_masked_gemm_workspace_bytes",
+            "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div",
+            "fgf8_testing_gemm_schedule"]
 
 
 class FGF8Error(RuntimeError):
@@ -80,6 +82,8 @@ def lib() -> ctypes.CDLL:
                                                    I64, I64, I64, P, SZ, P]
         L.fgf8_gemm_workspace_bytes.argtypes = [I64, I64, I64, I32]
         L.fgf8_gemm_workspace_bytes.restype = SZ
+        L.fgf8_gemm_workspace_min_bytes.argtypes = [I64, I64, I64, I32]
+        L.fgf8_gemm_workspace_min_bytes.restype = SZ
         L.fp8_masked_grouped_gemm_blockscaled.argtypes = [P, P, I64, P, P, I64, P, I32, I64, P, I64, ctypes.c_int,
                                                           I64, I64, P, SZ, P]
         L.fgf8_masked_gemm_workspace_bytes.argtypes = [I32, I64, I64, I64]
@@ -89,6 +93,7 @@ def lib() -> ctypes.CDLL:
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
         L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
         L.fgf8_selftest_scaled_div.argtypes = [P, P, I64, P, P, P]
+        L.fgf8_testing_gemm_schedule.argtypes = [I64, I64, I64, I32, SZ, I32, P]
         for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
                      "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc",
                      "fp8_grouped_gemm_blockscaled", "fgf8_read_status", "fgf8_mma_probe",
@@ -278,6 +283,17 @@ def fgf8_mma_probe(A: torch.Tensor, B: torch.Tensor, workspace: torch.Tensor | N
     st = lib().fgf8_mma_probe(_ptr(A), _ptr(B), _ptr(D), N, K, _ptr(ws), _stream(A.device))
     _check(st, "fgf8_mma_probe")
     return D
+
+
+def fgf8_testing_gemm_schedule(M: int, N: int, K: int, bkind: int = BSCALE_BLOCK128,
+                               ws_bytes: int | None = None, num_sms: int = 148) -> dict:
+    """The schedule fp8_gemm_blockscaled picks (host only, nothing launched).
+    ws_bytes defaults to fgf8_gemm_workspace_bytes(M, N, K, 1)."""
+    if ws_bytes is None:
+        ws_bytes = lib().fgf8_gemm_workspace_bytes(M, N, K, 1)
+    out = (ctypes.c_int32 * 4)()
+    _check(lib().fgf8_testing_gemm_schedule(M, N, K, bkind, ws_bytes, num_sms, out), "fgf8_testing_gemm_schedule")
+    return {"small_m": out[0], "bn": out[1], "dp_tiles": out[2], "tail_s": out[3]}
 
 
 def fgf8_read_status(workspace: torch.Tensor):

@@ -73,7 +73,7 @@ const char *fgf8_status_string(fgf8_status st)
 
 const char *fgf8_version(void)
 {
-    return "fgf8 0.6 sm_103a";
+    return "fgf8 0.7 sm_103a";
 }
 
 fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
@@ -151,6 +151,11 @@ size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_ex
     return fgf8::gemm_workspace_bytes(M, N, K, num_experts, 0);
 }
 
+size_t fgf8_gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts)
+{
+    return fgf8::gemm_workspace_min_bytes(M, N, K, num_experts);
+}
+
 static fgf8_status check_gemm(const uint8_t *A, const float *sa, int64_t ldsa, const uint8_t *B, const float *sb,
                               int64_t ldsb, int bkind, void *C, int64_t ldc, int cdt, int64_t M, int64_t N,
                               int64_t K, void *workspace, size_t ws_bytes, int32_t num_experts)
@@ -169,7 +174,7 @@ static fgf8_status check_gemm(const uint8_t *A, const float *sa, int64_t ldsa, c
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(C, 16) ||
         (ldc * esz) % 16 != 0 || !aligned(workspace, 256))
         return FGF8_ERR_MISALIGNED;
-    if (ws_bytes < fgf8::gemm_workspace_bytes(M, N, K, num_experts, 0)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < fgf8::gemm_workspace_min_bytes(M, N, K, num_experts)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
     return FGF8_OK;
 }
 
@@ -223,7 +228,7 @@ fgf8_status fp8_gemm_bf16a_blockscaled(const void *x, int64_t ldx, const uint8_t
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(B, 16) || !aligned(sb, 16) || !aligned(C, 16) ||
         (ldc * esz) % 16 != 0 || !aligned(workspace, 256))
         return FGF8_ERR_MISALIGNED;
-    if (ws_bytes < fgf8::gemm_workspace_bytes(M, N, K, 1, 0)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < fgf8::gemm_workspace_min_bytes(M, N, K, 1)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
     int num_sms = 0;
     fgf8_status st = current_device(&num_sms);
     if (st != FGF8_OK) return st;
@@ -311,7 +316,7 @@ fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int6
                                          int64_t ldc, fgf8_out_dtype cdt, int64_t M, int64_t N, int64_t K,
                                          void *stream)
 {
-    if (M >= 1 && N >= 1 && K >= 1 && fgf8::gemm_workspace_bytes(M, N, K, 1, 0) > kStaticScratchBytes)
+    if (M >= 1 && N >= 1 && K >= 1 && fgf8::gemm_workspace_min_bytes(M, N, K, 1) > kStaticScratchBytes)
         return FGF8_ERR_WORKSPACE_TOO_SMALL;
     int num_sms = 0;
     fgf8_status st = current_device(&num_sms);
@@ -373,6 +378,25 @@ fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, 
     fgf8_status st = current_device(nullptr);
     if (st != FGF8_OK) return st;
     return from_cuda(fgf8::launch_scaled_div_selftest(x, s, n, q_encoder, q_ieee, static_cast<cudaStream_t>(stream)));
+}
+
+fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t bkind, size_t ws_bytes,
+                                       int32_t num_sms, int32_t *schedule)
+{
+    if (M < 1 || N < 1 || K < 128 || K % 128 != 0 || (bkind != 0 && bkind != 1) || num_sms < 1 || !schedule)
+        return FGF8_ERR_INVALID_ARG;
+    fgf8::GemmArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.bkind = bkind;
+    a.ws_bytes = ws_bytes;
+    const fgf8::GemmSchedule g = fgf8::gemm_schedule(a, num_sms);
+    schedule[0] = g.small_m;
+    schedule[1] = g.bn;
+    schedule[2] = g.dp_tiles;
+    schedule[3] = g.tail_s;
+    return FGF8_OK;
 }
 
 }  // extern "C"

@@ -83,6 +83,41 @@ struct Params {
     const float *sa;                    // scales, copied by the scale warp with cp.async
     const float *sb;
     int64_t ldsa, ldsb;
+    // Tail split: tiles [0, dp_tiles) run whole, tile t on CTA t mod G; the
+    // other R = num_tiles - dp_tiles tiles (fewer than G) are each cut into
+    // tail_s contiguous K-group pieces, unit v = piece * R + tail tile on CTA v,
+    // so the last wave keeps every SM busy.  The last piece of a tail tile to
+    // finish adds the FP32 partials in piece (K) order.  Without a tail,
+    // dp_tiles = num_tiles and tail_units = 0.
+    int32_t dp_tiles, tail_s, tail_units;
+    float *tail_partials;               // [R * tail_s][BN / 4][128][4]
+    uint32_t *tail_tickets;             // [R], zero between calls
+};
+
+// The segments (tile, K groups k0..k1, tail piece or -1) one CTA processes, in
+// order; every role of the CTA walks the same sequence.
+struct SegIter {
+    int32_t t, v;
+    __device__ __forceinline__ SegIter() : t((int32_t)blockIdx.x), v((int32_t)blockIdx.x) {}
+    __device__ __forceinline__ bool next(const Params &p, int32_t &tile, int32_t &k0, int32_t &k1, int32_t &piece)
+    {
+        if (t < p.dp_tiles) {
+            tile = t;
+            k0 = 0;
+            k1 = p.KB;
+            piece = -1;
+            t += gridDim.x;
+            return true;
+        }
+        if (v >= p.tail_units) return false;
+        const int32_t R = p.num_tiles - p.dp_tiles;
+        piece = v / R;
+        tile = p.dp_tiles + (v - piece * R);
+        k0 = piece * p.KB / p.tail_s;
+        k1 = (piece + 1) * p.KB / p.tail_s;
+        v += gridDim.x;
+        return true;
+    }
 };
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a)
@@ -166,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = tm_full + 4;
     uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::off_misc + 4);
+    volatile int *tail_last = reinterpret_cast<volatile int *>(smem + L::off_misc + 8);
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
@@ -193,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_slot;
 
-    const int32_t KB = p.KB;
     if (warp < kEpiWarp0) regs_decrease<kCtrlRegs>();
 
     if (warp == kProducerWarp) {
@@ -202,13 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmB);
             uint32_t it = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            SegIter si;
+            int32_t tile, kbeg, kend, piece;
+            while (ok && si.next(p, tile, kbeg, kend, piece)) {
                 int32_t mb, nb;
                 tile_coords(tile, p, mb, nb);
                 const int32_t e = block_expert(p, mb);
                 if (e < 0) continue;
                 const int32_t b_row = (int32_t)(e * p.b_rows_per_expert) + nb * BN;
-                for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+                for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
                         record_timeout(p.status, kSiteProducerEmpty);
@@ -237,14 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // scale row are zero-filled without a read.
         uint32_t it = 0;
         bool ok = true;
-        for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        SegIter si;
+        int32_t tile, kbeg, kend, piece;
+        while (ok && si.next(p, tile, kbeg, kend, piece)) {
             int32_t mb, nb;
             tile_coords(tile, p, mb, nb);
             const int32_t e = block_expert(p, mb);
             if (e < 0) continue;
             const int64_t s_row0 = (int64_t)e * p.sb_rows_per_expert;
             const int64_t sa_x = (int64_t)mb * BM + 4 * lane;
-            for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+            for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
                 const uint32_t j = it % SC, phj = (it / SC) & 1;
                 if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
                     record_timeout(p.status, kSiteProducerScale);
@@ -274,11 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc = idesc_e4m3_f32(BM, BN);
         uint32_t it = 0;
         bool ok = true;
-        for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        SegIter si;
+        int32_t tile, kbeg, kend, piece;
+        while (ok && si.next(p, tile, kbeg, kend, piece)) {
             int32_t mb, nb;
             tile_coords(tile, p, mb, nb);
             if (block_expert(p, mb) < 0) continue;
-            for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+            for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                 const uint32_t buf = it & 1, phb = (it >> 1) & 1;
                 if (!mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
@@ -323,7 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t col0 = half * HALF;
         uint32_t it = 0;
         bool ok = true;
-        for (int32_t tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        // After a failed wait a warp still walks its remaining segments (without
+        // waiting), so that all eight reach the tail's named barrier together.
+        SegIter si;
+        int32_t tile, kbeg, kend, piece;
+        while (si.next(p, tile, kbeg, kend, piece)) {
             int32_t mb, nb;
             tile_coords(tile, p, mb, nb);
             if (block_expert(p, mb) < 0) continue;
@@ -331,11 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < HALF / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
             const int sb_sel = ROW_SB ? 0 : ((nb * BN / 128) & 3) + (int)(col0 / 128);
-            for (int32_t kb = 0; kb < KB; ++kb, ++it) {
+            for (int32_t kb = kbeg; ok && kb < kend; ++kb, ++it) {
                 const uint32_t j = it % SC, phj = (it / SC) & 1;
                 if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
                     record_timeout(p.status, kSiteEpiScale);
                     ok = false;
+                    *abort_flag = 1;
                     break;
                 }
                 const float sa_v = sm_sa[j * BM + row];
@@ -347,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
                     record_timeout(p.status, kSiteEpiTmemFull);
                     ok = false;
+                    *abort_flag = 1;
                     break;
                 }
                 tc_fence_after_sync();
@@ -385,7 +432,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&sc_empty[j]);
                 }
             }
-            if (!ok) break;
+            if (piece >= 0) {
+                // A piece of a tail tile: store the FP32 partial, take a ticket;
+                // the last piece to arrive adds all of them in K order.
+                const int32_t ti = tile - p.dp_tiles;
+                if (ok) {
+                    float *mine = p.tail_partials + (int64_t)(ti * p.tail_s + piece) * (BM * BN);
+#pragma unroll
+                    for (int c = 0; c < HALF; c += 4)
+                        *reinterpret_cast<float4 *>(mine + ((int64_t)((col0 + c) / 4) * BM + row) * 4) =
+                            make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
+                }
+                __threadfence();
+                const bool all_ok = named_barrier_and(1, kEpiWarps * 32, ok && !*abort_flag);
+                if (all_ok && threadIdx.x == kEpiWarp0 * 32) {
+                    const uint32_t ticket = atomicAdd(p.tail_tickets + ti, 1u);
+                    const int last = ticket == (uint32_t)(p.tail_s - 1);
+                    if (last) p.tail_tickets[ti] = 0u;          // ready for the next call
+                    *tail_last = last;
+                }
+                named_barrier_sync(1, kEpiWarps * 32);
+                if (!all_ok) ok = false;
+                if (!all_ok || !*tail_last) continue;
+                __threadfence();
+                const float *part = p.tail_partials + (int64_t)ti * p.tail_s * (BM * BN);
+#pragma unroll
+                for (int c = 0; c < HALF; c += 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + ((int64_t)((col0 + c) / 4) * BM + row) * 4));
+                    acc[c / 2] = make_float2(v.x, v.y);
+                    acc[c / 2 + 1] = make_float2(v.z, v.w);
+                }
+                for (int32_t q = 1; q < p.tail_s; ++q) {
+                    const float *pq = part + (int64_t)q * (BM * BN);
+#pragma unroll
+                    for (int c = 0; c < HALF; c += 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pq + ((int64_t)((col0 + c) / 4) * BM + row) * 4));
+                        acc[c / 2].x += v.x;
+                        acc[c / 2].y += v.y;
+                        acc[c / 2 + 1].x += v.z;
+                        acc[c / 2 + 1].y += v.w;
+                    }
+                }
+            } else if (!ok) {
+                continue;
+            }
             // write this thread's finished row segment
             const int64_t m = (int64_t)mb * BM + row;
             bool write = m < p.M;
@@ -1008,14 +1098,40 @@ int small_splits(int64_t N, int64_t K, int num_sms)
     return S < 1 ? 1 : (int)S;
 }
 
-size_t round256(size_t v)
+// Split count of the masked layout and the stream-K partial slots, from the
+// B300's 148 SMs rather than the device's, so that the workspace size a caller
+// queries and the launch agree.
+constexpr int kNominalSms = 148;
+
+// Last-wave split of a dense GEMM: with W = tiles / G whole waves, the
+// R = tiles mod G tail tiles are cut into s K pieces each (R * s <= G, one
+// round).  Cost in K-group steps of one tile: ceil(KB / s) for the pieces,
+// plus about two steps per 128 x BN FP32 partial that the last piece reads
+// back from L2 and one to store its own; s = 1 (no split) costs KB.
+struct TailPlan {
+    int32_t dp_tiles, s;
+    int64_t cost;               // K-group steps of the whole schedule on one CTA
+};
+
+TailPlan plan_tail(const GemmArgs &a, int64_t tiles, int64_t KB, int G, bool ws_ok)
 {
-    return (v + 255) / 256 * 256;
+    const int64_t W = tiles / G, R = tiles % G;
+    TailPlan t{(int32_t)tiles, 1, (W + (R > 0 ? 1 : 0)) * KB};
+    if (a.m_indices != nullptr || a.counts != nullptr || R == 0 || !ws_ok) return t;
+    for (int64_t s = 2; s <= KB && R * s <= G; ++s) {
+        const int64_t c = W * KB + (KB + s - 1) / s + 2 * s + 1;
+        if (c < t.cost) t = TailPlan{(int32_t)(W * G), (int32_t)s, c};
+    }
+    return t;
 }
 
-// Split count of the masked layout, from the B300's 148 SMs rather than the
-// device's, so that the workspace size a caller queries and the launch agree.
-constexpr int kNominalSms = 148;
+// Status header, counters (one per tail tile, fewer than 148) and up to 148
+// FP32 partial tiles of 128 x BN.
+static_assert(kNominalSms <= kMaxCounters, "one counter per tail tile");
+size_t tail_workspace_bytes(int BN)
+{
+    return kWsPartialsOffset + (size_t)kNominalSms * BM * BN * 4;
+}
 int masked_splits(int32_t E, int64_t n_tiles, int64_t KB)
 {
     int64_t S = kNominalSms / ((int64_t)E * n_tiles);
@@ -1028,14 +1144,21 @@ int masked_splits(int32_t E, int64_t n_tiles, int64_t KB)
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int)
 {
+    size_t bytes = gemm_workspace_min_bytes(M, N, K, num_experts);
+    // room for the last-wave split with 128 x 256 tiles
+    if (num_experts <= 1 && tail_workspace_bytes(256) > bytes) bytes = tail_workspace_bytes(256);
+    return bytes;
+}
+
+size_t gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts)
+{
     size_t bytes = kWsHeaderBytes;
     if (num_experts <= 1 && M <= 256) {
         // small-M split-K: arrival tickets and FP32 partials, sized for the
         // largest split count any device could choose
         const int64_t tiles = (N + BM - 1) / BM;
         const int64_t smax = K / BK < kMaxSplits ? K / BK : kMaxSplits;
-        bytes += round256((size_t)tiles * 4);
-        bytes += (size_t)tiles * smax * small_nt(M) * BM * 4;
+        bytes = kWsPartialsOffset + (size_t)tiles * smax * small_nt(M) * BM * 4;
     }
     return bytes;
 }
@@ -1044,21 +1167,18 @@ size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64
 {
     const int64_t tiles = (N + BM - 1) / BM;
     const int S = masked_splits(num_experts, tiles, K / BK);
-    size_t bytes = kWsHeaderBytes + round256((size_t)num_experts * tiles * 4);
-    if (S > 1) bytes += (size_t)num_experts * tiles * S * small_nt(cap) * BM * 4;
-    return bytes;
+    return S > 1 ? kWsPartialsOffset + (size_t)num_experts * tiles * S * small_nt(cap) * BM * 4 : kWsHeaderBytes;
 }
 
-size_t masked_workspace_zeroed_bytes(int32_t num_experts, int64_t N)
+size_t masked_workspace_zeroed_bytes(int32_t, int64_t)
 {
-    return kWsHeaderBytes + round256((size_t)num_experts * ((N + BM - 1) / BM) * 4);
+    return kWsPartialsOffset;
 }
 
-size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t, int32_t num_experts)
+size_t gemm_workspace_zeroed_bytes(int64_t, int64_t, int64_t, int32_t)
 {
-    size_t bytes = kWsHeaderBytes;
-    if (num_experts <= 1 && M <= 256) bytes += round256((size_t)((N + BM - 1) / BM) * 4);
-    return bytes;
+    // status word and the arrival counters
+    return kWsPartialsOffset;
 }
 
 namespace {
@@ -1091,9 +1211,21 @@ Params make_params(const GemmArgs &a)
 template <int BN, int STAGES>
 cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
-    const Params p = make_params<BN>(a);
-    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    Params p = make_params<BN>(a);
+    int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
+    const int G = num_sms < kNominalSms ? num_sms : kNominalSms;
+    const TailPlan t = plan_tail(a, p.num_tiles, p.KB, G, a.ws_bytes >= tail_workspace_bytes(BN));
+    p.dp_tiles = t.dp_tiles;
+    if (t.s > 1) {
+        const int32_t units = (p.num_tiles - t.dp_tiles) * t.s;
+        grid = t.dp_tiles > 0 ? G : units;
+        p.tail_s = t.s;
+        p.tail_units = units;
+        uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+        p.tail_tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
+        p.tail_partials = reinterpret_cast<float *>(ws + kWsPartialsOffset);
+    }
     if (a.bkind == 1)
         return a.out_f32 ? launch_variant<BN, STAGES, 12, true, true>(a, p, grid, stream)
                          : launch_variant<BN, STAGES, 12, true, false>(a, p, grid, stream);
@@ -1113,6 +1245,7 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     p.n_tiles = (int32_t)((a.N + BM - 1) / BM);
     const int32_t E = a.counts != nullptr ? a.num_experts : 1;
     p.S = a.counts != nullptr ? masked_splits(E, p.n_tiles, p.KB) : small_splits(a.N, a.K, num_sms);
+    if ((int64_t)E * p.n_tiles > kMaxCounters) p.S = 1;    // no counters needed without a split
     p.C = a.C;
     p.ldc = a.ldc;
     p.counts = a.counts;
@@ -1122,7 +1255,7 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     p.status = reinterpret_cast<DeviceStatus *>(ws);
     p.tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
-    p.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + round256((size_t)E * p.n_tiles * 4));
+    p.partials = reinterpret_cast<float *>(ws + kWsPartialsOffset);
     CUtensorMap tmW, tmX, tmSA, tmSB;
     memset(&tmSA, 0, sizeof(tmSA));
     memset(&tmSB, 0, sizeof(tmSB));
@@ -1160,14 +1293,32 @@ cudaError_t launch_small_nt(const GemmArgs &a, cudaStream_t stream, int num_sms)
 // enough better to pay for their lower per-tile efficiency.
 int choose_bn(const GemmArgs &a, int num_sms)
 {
-    const int64_t mb = (a.M + BM - 1) / BM;
-    const int64_t t256 = mb * ((a.N + 255) / 256), t128 = mb * ((a.N + 127) / 128);
-    const double w256 = (double)((t256 + num_sms - 1) / num_sms) * 2.0;
-    const double w128 = (double)((t128 + num_sms - 1) / num_sms) * 1.15;
-    return w128 < w256 ? 128 : 256;
+    // K-group steps on one CTA, a 128 x 256 step costing about 2 / 1.15 times
+    // a 128 x 128 one
+    const int G = num_sms < kNominalSms ? num_sms : kNominalSms;
+    const int64_t mb = (a.M + BM - 1) / BM, KB = a.K / BK;
+    const TailPlan t256 = plan_tail(a, mb * ((a.N + 255) / 256), KB, G, a.ws_bytes >= tail_workspace_bytes(256));
+    const TailPlan t128 = plan_tail(a, mb * ((a.N + 127) / 128), KB, G, a.ws_bytes >= tail_workspace_bytes(128));
+    return (double)t128.cost * 1.15 < (double)t256.cost * 2.0 ? 128 : 256;
 }
 
 }  // namespace
+
+GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
+{
+    GemmSchedule g{};
+    if (a.m_indices == nullptr && a.bkind == 0 && use_small_m(a.M, a.N, 1, num_sms)) {
+        g.small_m = 1;
+        return g;
+    }
+    g.bn = choose_bn(a, num_sms);
+    const int G = num_sms < kNominalSms ? num_sms : kNominalSms;
+    const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + g.bn - 1) / g.bn);
+    const TailPlan t = plan_tail(a, tiles, a.K / BK, G, a.ws_bytes >= tail_workspace_bytes(g.bn));
+    g.dp_tiles = t.dp_tiles;
+    g.tail_s = t.s;
+    return g;
+}
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {

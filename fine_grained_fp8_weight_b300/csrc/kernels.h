@@ -47,14 +47,28 @@ struct GemmArgs {
     int64_t ldx = 0;
 };
 
-// Workspace layout: [0, 256) status word; then, for small M, the split-K
-// arrival counters (one per 128 weight rows) and the FP32 partial sums.
+// Workspace layout, the same for every GEMM kernel so that one workspace can
+// serve all of them in turn: [0, 256) status word; [256, 1280) 256 arrival
+// counters, written by nothing but the split kernels' atomics and their
+// resets to zero (small-M split-K: one per 128 weight rows and expert; the
+// last-wave split: one per tail tile); from 1280 on, FP32 partial sums.
 constexpr size_t kWsHeaderBytes = 256;
+constexpr int kMaxCounters = 256;
+constexpr size_t kWsPartialsOffset = kWsHeaderBytes + kMaxCounters * 4;
 
+// Workspace that enables every schedule (for dense GEMMs, the last-wave
+// split's partial tiles), and the least a call accepts.
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int num_sms);
+size_t gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 // Leading part of the workspace that must be zero when a call starts (the
 // status word and the split-K arrival counters).
 size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
+// The schedule launch_gemm picks: small-M kernel, or tile width, whole-tile
+// count and pieces per last-wave tile (1: no split).
+struct GemmSchedule {
+    int small_m, bn, dp_tiles, tail_s;
+};
+GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms);
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
 // Masked grouped layout: scratch size, its zero-initialised prefix, launch.
 size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);

@@ -161,13 +161,21 @@ fgf8_status fp8_quant_w_128x128_t(const void *w, int64_t N, int64_t K, int64_t l
  *        ldsb % 4 == 0.
  *   C  : [M][ldc] BF16 (cdt = FGF8_OUT_BF16) or FP32 (FGF8_OUT_FP32); ldc >= N,
  *        ldc * element size % 16 == 0, 16-byte aligned.
- *   workspace : device scratch of at least fgf8_gemm_workspace_bytes(M, N, K, 1)
- *        bytes, 256-byte aligned, ZERO-FILLED before its first use.  It holds
- *        the device status word and, for small M, the split-K partial sums
- *        and arrival counters.  The kernels leave it ready for the next call
- *        (counters back at zero) unless a call reports FGF8_ERR_TIMEOUT, after
- *        which it must be zero-filled again.  One workspace must not be used
- *        by two calls that can run at the same time.
+ *   workspace : device scratch of at least fgf8_gemm_workspace_min_bytes(M, N,
+ *        K, 1) bytes, 256-byte aligned, ZERO-FILLED before its first use.  It
+ *        holds the device status word and, for small M, the split-K partial
+ *        sums and arrival counters.  With fgf8_gemm_workspace_bytes(M, N, K, 1)
+ *        bytes it also holds the last-wave split: when the output tiles leave
+ *        the last wave over the SMs partly empty, those tail tiles are cut
+ *        along K into pieces that run on the idle SMs, and the last piece of
+ *        each adds the FP32 partials in K order.  The result is then the same
+ *        sum grouped differently (it can differ from the whole-tile schedule
+ *        in the last bits, within the error bound), and it is the same on
+ *        every call with the same shape and workspace size.  The kernels leave
+ *        the workspace ready for the next call (counters back at zero) unless
+ *        a call reports FGF8_ERR_TIMEOUT, after which it must be zero-filled
+ *        again.  One workspace must not be used by two calls that can run at
+ *        the same time.
  */
 fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa,
                                  const uint8_t *B, const float *sb, int64_t ldsb,
@@ -192,8 +200,9 @@ fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress) with the device current; make that first call
  *     before any stream capture on the device.
- *   - Shapes whose scratch need (fgf8_gemm_workspace_bytes(M, N, K, 1)) exceeds
- *     1 MiB are rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *   - Shapes whose scratch need (fgf8_gemm_workspace_min_bytes(M, N, K, 1))
+ *     exceeds 1 MiB are rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any
+ *     launch.  The 1 MiB never holds the last-wave split: whole tiles only.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; each call clears the part that must start at zero (the device
  *     status word and, for M <= 256, the split-K arrival counters) on `stream`
@@ -222,7 +231,7 @@ fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int6
  *   B  : E4M3 [N][K] with 128x128 block scales sb [K/128][ldsb] as in
  *        fp8_gemm_blockscaled (BLOCK128 kind).  N % 16 == 0, K % 128 == 0.
  *   C  : [M][ldc] BF16 or FP32, as in fp8_gemm_blockscaled.
- *   workspace : at least fgf8_gemm_workspace_bytes(M, N, K, 1) bytes, as in
+ *   workspace : at least fgf8_gemm_workspace_min_bytes(M, N, K, 1) bytes, as in
  *        fp8_gemm_blockscaled.  M == 0 or N == 0 is a no-op.
  */
 fgf8_status fp8_gemm_bf16a_blockscaled(const void *x, int64_t ldx, const uint8_t *B, const float *sb, int64_t ldsb,
@@ -291,8 +300,11 @@ fgf8_status fp8_masked_grouped_gemm_blockscaled(const uint8_t *A, const float *s
 /* Workspace bytes fp8_masked_grouped_gemm_blockscaled needs for these sizes. */
 size_t fgf8_masked_gemm_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);
 
-/* Workspace size (bytes) needed by the GEMM entry points for this shape. */
+/* Workspace size (bytes) with which the GEMM entry points can use every
+ * schedule for this shape (for dense GEMMs, the last-wave split, about
+ * 19 MiB), and the least they accept (FGF8_ERR_WORKSPACE_TOO_SMALL below it). */
 size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
+size_t fgf8_gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 
 /*
  * fgf8_read_status -- synchronizes `stream`, then returns the device status

@@ -36,6 +36,21 @@ fgf8_status fgf8_selftest_wait_timeout(void *workspace, uint32_t budget_us, void
 fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, float *q_encoder,
                                      float *q_ieee, void *stream);
 
+/*
+ * fgf8_testing_gemm_schedule -- host only, launches nothing: the schedule that
+ * fp8_gemm_blockscaled picks for a dense M x N x K GEMM with B scales of
+ * `bkind` (0 block, 1 per row), a workspace of `ws_bytes` and `num_sms` SMs:
+ *   schedule[0] = 1 if the small-M kernel runs (the rest is then 0);
+ *   schedule[1] = output tile width (128 or 256 columns, 128 rows);
+ *   schedule[2] = tiles computed whole (a multiple of min(num_sms, 148) when
+ *                 the last wave is split, else all of them);
+ *   schedule[3] = K pieces per remaining tile (1 = no split).
+ * `schedule` points to 4 host int32.  Lets tests check the schedule choice on
+ * a CPU and confirm that a GPU case covers the path it is meant to.
+ */
+fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t bkind, size_t ws_bytes,
+                                       int32_t num_sms, int32_t *schedule);
+
 #ifdef __cplusplus
 }
 #endif

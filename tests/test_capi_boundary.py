@@ -115,3 +115,64 @@ def test_probe_rejects(L):
 
 def test_workspace_size(L):
     assert L.fgf8_gemm_workspace_bytes(4096, 18432, 7168, 1) >= 256
+    assert L.fgf8_gemm_workspace_min_bytes(4096, 18432, 7168, 1) >= 256
+    # the recommended size holds the last-wave split, the least does not need to
+    for shape in [(4096, 18432, 7168), (4096, 7168, 18432), (16, 4096, 7168), (384, 3072, 1792)]:
+        assert L.fgf8_gemm_workspace_bytes(*shape, 1) >= L.fgf8_gemm_workspace_min_bytes(*shape, 1)
+    assert L.fgf8_gemm_workspace_min_bytes(4096, 7168, 18432, 1) <= 1 << 20
+
+
+# --- schedule choice (host only) ---
+
+def _tiles(M, N, bn):
+    return -(-M // 128) * -(-N // bn)
+
+
+@pytest.mark.parametrize("sms", [148, 132, 64])
+def test_last_wave_split_invariants(L, sms):
+    """Whole tiles fill whole waves over min(SMs, 148) CTAs; the rest (fewer
+    than that) are cut into s <= K/128 pieces that fit one more wave."""
+    G = min(sms, 148)
+    seen_split = 0
+    for M in (257, 384, 1000, 1280, 2560, 4096, 7168):
+        for N in (512, 1792, 3072, 4096, 7168, 18432):
+            for K in (128, 1024, 2048, 7168, 18432):
+                sch = fg.fgf8_testing_gemm_schedule(M, N, K, 0, num_sms=sms)
+                if sch["small_m"]:
+                    continue
+                tiles = _tiles(M, N, sch["bn"])
+                if sch["tail_s"] == 1:
+                    assert sch["dp_tiles"] == tiles
+                    continue
+                seen_split += 1
+                R = tiles - sch["dp_tiles"]
+                assert sch["dp_tiles"] % G == 0 and 0 < R < G
+                assert 2 <= sch["tail_s"] <= K // 128 and R * sch["tail_s"] <= G
+                # with the least workspace the same GEMM runs whole tiles only
+                wmin = fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1)
+                plain = fg.fgf8_testing_gemm_schedule(M, N, K, 0, ws_bytes=wmin, num_sms=sms)
+                assert plain["tail_s"] == 1 and plain["dp_tiles"] == _tiles(M, N, plain["bn"])
+    assert seen_split > 10
+
+
+def test_schedule_of_the_prefill_pair_and_wgrad(L):
+    # 4096 x 7168 x 18432: 896 tiles of 128 x 256 = 6 waves + 8; the 8 run as
+    # 8 K pieces each (18 K groups per piece) next to the 6 whole waves
+    assert fg.fgf8_testing_gemm_schedule(4096, 7168, 18432) == {"small_m": 0, "bn": 256, "dp_tiles": 888, "tail_s": 8}
+    # 4096 x 18432 x 7168: 2304 tiles = 15 waves + 84; splitting 84 tiles
+    # cannot fill a wave better than whole tiles do
+    assert fg.fgf8_testing_gemm_schedule(4096, 18432, 7168)["tail_s"] == 1
+    # weight gradient 7168 x 2048 x 8192 (per-row B scales): 448 tiles = 3 waves + 4
+    sch = fg.fgf8_testing_gemm_schedule(7168, 2048, 8192, 1)
+    assert sch["bn"] == 256 and sch["dp_tiles"] == 444 and sch["tail_s"] > 1
+    assert fg.fgf8_testing_gemm_schedule(16, 4096, 7168)["small_m"] == 1
+
+
+def test_schedule_rejects(L):
+    out = (ctypes.c_int32 * 4)()
+    f = L.fgf8_testing_gemm_schedule
+    assert f(0, 128, 128, 0, 1 << 20, 148, out) == 1
+    assert f(128, 128, 100, 0, 1 << 20, 148, out) == 1
+    assert f(128, 128, 128, 2, 1 << 20, 148, out) == 1
+    assert f(128, 128, 128, 0, 1 << 20, 0, out) == 1
+    assert f(128, 128, 128, 0, 1 << 20, 148, None) == 1

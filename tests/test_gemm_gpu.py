@@ -27,13 +27,21 @@ def _sample_rows(M, n, seed):
     return np.sort(np.random.default_rng(seed).choice(M, size=min(n, M), replace=False))
 
 
-def _run_dense(Abits, Bbits, out_dtype, rows=None, bkind=0):
+def _rows_per_block(M, n, seed):
+    """n random rows of every 128-row block (all rows of a shorter last block)."""
+    rng = np.random.default_rng(seed)
+    return np.concatenate([np.sort(rng.choice(np.arange(m0, min(m0 + 128, M)), size=min(n, M - m0), replace=False))
+                           for m0 in range(0, M, 128)])
+
+
+def _run_dense(Abits, Bbits, out_dtype, rows=None, bkind=0, workspace=None):
     qa, sa = oracle.quant_act_1x128(Abits)
     if bkind == 0:
         qb, sb = oracle.quant_w_128x128(Bbits)
     else:
         qb, sb = oracle.quant_act_1x128(Bbits)          # per-row (1x128) B scales
-    C = fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), bkind=bkind, out_dtype=out_dtype)
+    C = fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), bkind=bkind, out_dtype=out_dtype,
+                                workspace=workspace)
     torch.cuda.synchronize()
     Cg = bf16_out_to_f64(C) if out_dtype == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
     Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb, bkind, rows=rows)
@@ -73,6 +81,51 @@ def test_dense_large_m(M, N, K, out):
     dt = torch.bfloat16 if out == "bf16" else torch.float32
     Cg, Cr, S = _run_dense(A, B, dt)
     assert_within_bound(Cg, Cr, S, f"{M}x{N}x{K}")
+
+
+# Last-wave split: tiles left over after the whole waves are cut along K and
+# the last piece of each adds the FP32 partials.  Cases: no whole wave (every
+# tile split), one and two whole waves, both tile widths, both B-scale kinds,
+# both output types.  The same GEMM with the least workspace runs whole tiles
+# only; both schedules must meet the bound.  The oracle takes sampled rows of
+# every 128-row block (two, one on the largest shapes), so every output tile
+# is checked.
+_split_cases = {}
+
+
+def _split_case(M, N, K, bkind):
+    """Quantized operands, sampled rows and the oracle's result, once per shape
+    (the oracle is the slow part; both output types and schedules reuse it)."""
+    key = (M, N, K, bkind)
+    if key not in _split_cases:
+        rng = np.random.default_rng(M * 3 + N + K + bkind)
+        A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+        B = wl.bf16_normal(rng, (N, K), 0.02)
+        qa, sa = oracle.quant_act_1x128(A)
+        qb, sb = oracle.quant_w_128x128(B) if bkind == 0 else oracle.quant_act_1x128(B)
+        rows = _rows_per_block(M, 1 if M * K > 4_000_000 else 2, M + K)
+        Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb, bkind, rows=rows)
+        _split_cases[key] = ([_d(t) for t in (qa, sa, qb, sb)], rows, Cr, S)
+    return _split_cases[key]
+
+
+@pytest.mark.parametrize("M,N,K,bkind,bn", [(384, 3072, 1792, 0, 128), (1280, 4096, 2048, 0, 128),
+                                            (2560, 4096, 4096, 0, 256), (1280, 4096, 2048, 1, 128),
+                                            (2560, 4096, 4096, 1, 256)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_last_wave_split(M, N, K, bkind, bn, out):
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    sch = fg.fgf8_testing_gemm_schedule(M, N, K, bkind, num_sms=sm)
+    assert sch["bn"] == bn and sch["tail_s"] > 1, sch
+    ops, rows, Cr, S = _split_case(M, N, K, bkind)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    ws_min = torch.zeros(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), dtype=torch.uint8, device=DEV)
+    assert fg.fgf8_testing_gemm_schedule(M, N, K, bkind, ws_bytes=ws_min.numel(), num_sms=sm)["tail_s"] == 1
+    for label, ws in (("split", None), ("whole tiles", ws_min)):
+        C = fg.fp8_gemm_blockscaled(*ops, bkind=bkind, out_dtype=dt, workspace=ws)
+        torch.cuda.synchronize()
+        Cg = bf16_out_to_f64(C) if dt == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
+        assert_within_bound(Cg[rows], Cr, S, f"{label} {M}x{N}x{K}")
 
 
 # M <= 256 takes the small-M path (weights on the MMA's M side, K split over
@@ -216,7 +269,8 @@ def test_full_size_wgrad_sampled():
 @pytest.mark.parametrize("M,N,K,bkind,out", [(2048, 4096, 4096, 0, "bf16"), (4096, 2048, 4096, 1, "fp32"),
                                              (4096, 2048, 4096, 1, "bf16"), (4096, 4096, 2048, 0, "fp32"),
                                              (3072, 1792, 2048, 1, "fp32"), (3072, 1792, 2048, 0, "bf16"),
-                                             (64, 7168, 4096, 0, "bf16"), (200, 2048, 4096, 0, "fp32")])
+                                             (64, 7168, 4096, 0, "bf16"), (200, 2048, 4096, 0, "fp32"),
+                                             (2560, 4096, 4096, 0, "bf16"), (1280, 4096, 2048, 1, "fp32")])
 def test_repeated_launches_bitwise_identical(M, N, K, bkind, out):
     g = torch.Generator(device="cpu").manual_seed(M + N + K + bkind)
     qa = torch.randint(0, 256, (M, K), dtype=torch.uint8, generator=g)
@@ -372,3 +426,30 @@ def test_bf16a_row_stride_and_rejects_large_m():
     assert torch.equal(fused.view(torch.int16), twostep.view(torch.int16))
     with pytest.raises(fg.FGF8Error, match="UNSUPPORTED_SHAPE"):
         fg.fp8_gemm_bf16a_blockscaled(dev_bf16(wl.bf16_normal(rng, (65, 512))), qb, sb)
+
+
+# One workspace serves every GEMM kernel in turn: the split kernels' arrival
+# counters sit in one region that no kernel writes partial sums into, so a
+# small-M split-K call, a masked call and a last-wave split call leave each
+# other's counters at zero.  Each result is checked against the oracle.
+def test_one_workspace_serves_every_kernel():
+    L = fg.lib()
+    need = max(L.fgf8_gemm_workspace_bytes(16, 1024, 2048, 1), L.fgf8_gemm_workspace_bytes(384, 3072, 1792, 1),
+               L.fgf8_masked_gemm_workspace_bytes(4, 64, 256, 1024))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    rng = np.random.default_rng(77)
+    small = (wl.bf16_normal(rng, (16, 2048), 1.0, 0.01, 100.0), wl.bf16_normal(rng, (1024, 2048), 0.02))
+    split = (wl.bf16_normal(rng, (384, 1792), 1.0, 0.01, 100.0), wl.bf16_normal(rng, (3072, 1792), 0.02))
+    w = wl.masked_small(9, [40, 0, 7, 64], 64, 256, 1024)
+    assert fg.fgf8_testing_gemm_schedule(16, 1024, 2048)["small_m"] == 1
+    assert fg.fgf8_testing_gemm_schedule(384, 3072, 1792)["tail_s"] > 1
+    for round_ in range(2):
+        for A, B in (small, split):
+            rows = _rows_per_block(A.shape[0], 2, round_)
+            Cg, Cr, S = _run_dense(A, B, torch.float32, rows=rows, workspace=ws)
+            assert_within_bound(Cg, Cr, S, f"{A.shape[0]}x{B.shape[0]} pass {round_}")
+        g, Cg, Cr, S = _run_masked(w, torch.float32, workspace=ws)
+        for e, c in enumerate(g.counts):
+            if c:
+                assert_within_bound(Cg[e, :c], Cr[e, :c], S[e, :c], f"masked expert {e} pass {round_}")
+    assert not bool(ws[256:1280].any()), "arrival counters left non-zero"
