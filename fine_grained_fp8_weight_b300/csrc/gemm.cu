@@ -22,6 +22,12 @@
 //     per thread, half of the tile's columns each) read each partial with
 //     tcgen05.ld, multiply by sa*sb and add into FP32 registers, then write
 //     the finished tile (BF16 or FP32).
+//   Schedule: tile t runs on CTA t mod grid.  When the tiles leave the last
+//   wave over the SMs partly empty (dense GEMMs, workspace permitting), the
+//   whole waves keep that order and each remaining tile is cut into K pieces
+//   on otherwise idle CTAs; the last piece to finish (an atomic ticket) adds
+//   the FP32 partials in K order and writes the tile.  No CTA waits for
+//   another.
 // gemm_smallm_kernel (decode, M <= 256 tokens): the weight tile takes the
 // MMA's M side and the tokens its N side, K is split over CTAs with an
 // in-order reduction; the same kernel serves the masked grouped layout
@@ -1098,7 +1104,7 @@ int small_splits(int64_t N, int64_t K, int num_sms)
     return S < 1 ? 1 : (int)S;
 }
 
-// Split count of the masked layout and the stream-K partial slots, from the
+// Split count of the masked layout and the last-wave split's grid, from the
 // B300's 148 SMs rather than the device's, so that the workspace size a caller
 // queries and the launch agree.
 constexpr int kNominalSms = 148;
