@@ -205,13 +205,22 @@ def job_tflops(flops_per_rank_step, world, ms_step):
 class DevicePath:
     """The step on device buffers: every op is one C-ABI call on one stream."""
 
-    def __init__(self, work, dev, fused_a=False):
+    def __init__(self, work, dev, fused_a=False, least_workspace=False):
         import torch
         import fine_grained_fp8_weight_b300 as fg
         from fine_grained_fp8_weight_b300 import workloads as wl
         from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Masked, Wgrad
         self.fg, self.torch, self.dev = fg, torch, dev
         self.ops = []          # (kind, name, callable, bytes or flops)
+
+        def gemm_ws(M, N, K):
+            # None: the library's recommended workspace (every schedule); else a
+            # workspace of the least accepted size (whole output tiles only)
+            if not least_workspace:
+                return None
+            return torch.zeros(max(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), 4096), dtype=torch.uint8,
+                               device=dev)
+
         self.inputs = []       # (host numpy bits, device tensor) for the end-to-end leg
         self.outputs = []
         for g in work.gemms:
@@ -242,8 +251,8 @@ class DevicePath:
                                  lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128(B)),
                                  qbytes(N, K, (N // 128 + 1) * K // 128)))
                 self.ops.append(("gemm", f"{g.name}.gemm",
-                                 lambda st=st, C=C: fg.fp8_gemm_blockscaled(st["a"][0], st["a"][1], st["b"][0],
-                                                                            st["b"][1], out=C),
+                                 lambda st=st, C=C, ws=gemm_ws(M, N, K): fg.fp8_gemm_blockscaled(
+                                     st["a"][0], st["a"][1], st["b"][0], st["b"][1], out=C, workspace=ws),
                                  gemm_flops(g)))
             elif isinstance(g, Grouped):
                 A = wl.bf16_bits_to_torch(g.A).to(dev)
@@ -298,8 +307,8 @@ class DevicePath:
                                  lambda W=W, st=st: st.update(b=fg.fp8_quant_w_128x128_t(W)),
                                  N * K * 3 + (N // 128) * (K // 128) * 4))
                 self.ops.append(("gemm", f"{g.name}.gemm",
-                                 lambda st=st, C=C: fg.fp8_gemm_blockscaled(st["a"][0], st["a"][1], st["b"][0],
-                                                                            st["b"][1], out=C),
+                                 lambda st=st, C=C, ws=gemm_ws(T, K, N): fg.fp8_gemm_blockscaled(
+                                     st["a"][0], st["a"][1], st["b"][0], st["b"][1], out=C, workspace=ws),
                                  gemm_flops(g)))
             elif isinstance(g, Wgrad):
                 dY = wl.bf16_bits_to_torch(g.dY).to(dev)
@@ -317,9 +326,9 @@ class DevicePath:
                                  lambda X=X, st=st: st.update(b=fg.fp8_quant_act_1x128(X, rows=False, transposed=True)),
                                  T * K * 3 + T * K // 32))
                 self.ops.append(("gemm", f"{g.name}.gemm",
-                                 lambda st=st, C=C: fg.fp8_gemm_blockscaled(st["a"][2], st["a"][3], st["b"][2],
-                                                                            st["b"][3], bkind=fg.BSCALE_ROW1x128,
-                                                                            out=C),
+                                 lambda st=st, C=C, ws=gemm_ws(N, K, T): fg.fp8_gemm_blockscaled(
+                                     st["a"][2], st["a"][3], st["b"][2], st["b"][3], bkind=fg.BSCALE_ROW1x128,
+                                     out=C, workspace=ws),
                                  gemm_flops(g)))
         self.gemm_flops = sum(w for k, _, _, w in self.ops if k == "gemm")
         self.gemm_bytes = {f"{g.name}.{'grouped_gemm' if isinstance(g, Grouped) else 'gemm'}": gemm_bytes(g)
@@ -346,7 +355,7 @@ def run_device(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     work = make_workload(args.workload)
-    path = DevicePath(work, dev, fused_a=args.fused_a)
+    path = DevicePath(work, dev, fused_a=args.fused_a, least_workspace=args.workspace == "least")
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
 
@@ -449,6 +458,7 @@ def run_device(args, rank, world, local_rank):
         "config": {"workload": work.name,
                    "gemms": [n for k, n, _, _ in path.ops if k == "gemm"],
                    "l2": "no flush: each step reads inputs larger than the 126 MB L2",
+                   "gemm_workspace": args.workspace,
                    "parallelism": f"replicas x{world}"},
         "roofline": ({"bound": "hbm", "achieved": per_op[dom_name]["GB/s"], "peak": peaks["hbm_gbs"],
                       "unit": "GB/s", "frac": per_op[dom_name]["frac_hbm"], "traffic": traffic,
@@ -627,6 +637,9 @@ def main():
     ap.add_argument("--profile-gemm", action="store_true")
     ap.add_argument("--gemm-index", type=int, default=0)
     ap.add_argument("--profile-op", default=None, help="run one op of the workload repeatedly (for ncu)")
+    ap.add_argument("--workspace", default="full", choices=["full", "least"],
+                    help="dense GEMM workspace: the recommended size (last-wave split allowed) or the least "
+                         "accepted size (whole output tiles only)")
     ap.add_argument("--fused-a", action="store_true",
                     help="GEMMs with at most 64 tokens quantize their BF16 tokens inside the GEMM")
     args = ap.parse_args()
