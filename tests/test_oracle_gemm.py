@@ -228,3 +228,23 @@ def test_masked_grouped_equals_contiguous_grouped():
         for r in range(int(counts[e])):
             assert np.array_equal(Cm[e, r], Cc[i + r]) and np.array_equal(Sm[e, r], Sc[i + r])
         i += pad
+
+
+def test_masked_counts_outside_the_slot_are_clamped():
+    # a count past the slot stands for the whole slot and a negative count for
+    # none (the masked GEMM's argument rule); exact sums as above
+    E, cap, N, K = 3, 32, 128, 256
+    counts = np.array([cap + 7, -2, 5], np.int32)
+    used = [cap, 0, 5]
+    av, A, bv, B, ja, jb, sa, sb = _masked_case(33, E, cap, N, K, counts)
+    C, S = oracle.masked_grouped_gemm_blockscaled(A, sa, B, sb, counts)
+    for e in range(E):
+        for m in range(cap):
+            if m >= used[e]:
+                assert np.all(np.isnan(C[e, m])) and np.all(S[e, m] == 0)
+                continue
+            ref = np.zeros(N)
+            for kb in range(K // 128):
+                part = (bv[e][:, kb * 128:(kb + 1) * 128] @ av[e, m, kb * 128:(kb + 1) * 128]).astype(np.float64)
+                ref += part * 2.0 ** ja[e, kb, m] * np.exp2(np.repeat(jb[e, kb], 128)[:N])
+            assert np.array_equal(C[e, m], ref)

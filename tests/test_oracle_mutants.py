@@ -2,11 +2,14 @@
 of the oracle source (a wrong constant, rounding rule, sign, index, dropped
 term or transposed operand) makes at least one pin test fail.
 
-Each mutant is compiled with the oracle's own flags and the pin tests run
+Each C mutant is compiled with the oracle's own flags and the pin tests run
 against it in a child process; the planted mistakes all stay within the
-buffers' bounds.
+buffers' bounds.  The oracle's Python layer (the masked layout's slot
+arithmetic, the W^T wrapper) gets the same treatment: a mutated copy of the
+package runs the pins in a scratch directory.
 """
 import os
+import shutil
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -42,6 +45,33 @@ MUTANTS = {
 }
 
 
+# Mistakes planted in the Python layer of the oracle (oracle/__init__.py).
+PY_MUTANTS = {
+    "masked_slot_column": ("[:, e * cap:(e + 1) * cap]", "[:, e:e + cap]"),
+    "masked_shared_expert_scales": ("B[e], sb[e], 0, rows=rows)", "B[e], sb[0], 0, rows=rows)"),
+    "masked_count_unclamped": ("c = int(min(max(int(counts[e]), 0), cap))", "c = int(counts[e])"),
+    "wt_not_transposed": ("np.ascontiguousarray(np.asarray(w_bits, np.uint16).T)",
+                          "np.ascontiguousarray(np.asarray(w_bits, np.uint16))"),
+}
+
+
+def _run_py_mutant(name, tmpdir):
+    before, after = PY_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert src.count(before) == 1, f"{name}: pattern must occur exactly once"
+    work = os.path.join(tmpdir, name)
+    os.makedirs(os.path.join(work, "oracle"))
+    with open(os.path.join(work, "oracle", "__init__.py"), "w") as f:
+        f.write(src.replace(before, after))
+    shutil.copy(os.path.join(ROOT, "oracle", "oracle.c"), os.path.join(work, "oracle"))
+    shutil.copytree(os.path.join(ROOT, "tests"), os.path.join(work, "tests"),
+                    ignore=shutil.ignore_patterns("__pycache__"))
+    env = dict(os.environ, FGF8_ORACLE_LIB=oracle.build())
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *PINS],
+                       cwd=work, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode, r.stdout[-400:]
+
+
 def _run_mutant(name, tmpdir):
     before, after = MUTANTS[name]
     src = open(os.path.join(ROOT, "oracle", "oracle.c")).read()
@@ -62,3 +92,20 @@ def test_every_planted_mistake_is_caught(tmp_path):
         results = list(ex.map(lambda n: _run_mutant(n, str(tmp_path)), MUTANTS))
     survivors = [(n, out) for n, rc, out in results if rc != 1]
     assert not survivors, f"mutants not caught (or crashed): {survivors}"
+
+
+def test_every_planted_python_mistake_is_caught(tmp_path):
+    with ThreadPoolExecutor(max_workers=min(4, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(lambda n: _run_py_mutant(n, str(tmp_path)), PY_MUTANTS))
+    survivors = [(n, out) for n, rc, out in results if rc != 1]
+    assert not survivors, f"mutants not caught (or crashed): {survivors}"
+
+
+def test_python_mutant_harness_passes_the_unmutated_oracle(tmp_path):
+    # the scratch-directory copy itself must not fail the pins
+    PY_MUTANTS["_identity"] = ("def round_up(v: int, m: int) -> int:", "def round_up(v: int, m: int) -> int:")
+    try:
+        name, rc, out = _run_py_mutant("_identity", str(tmp_path))
+    finally:
+        del PY_MUTANTS["_identity"]
+    assert rc == 0, out
