@@ -105,6 +105,76 @@ def test_grouped_rejects(L):
     assert f(*bad) == 1                      # no experts
 
 
+def test_quant_w_grouped_and_transposed_reject(L):
+    g = L.fp8_quant_w_128x128_grouped
+    assert g(A16, -1, 256, 128, 128, A16, A16, 4, None) == 1          # negative expert count
+    assert g(A16, 2, 256, 200, 200, A16, A16, 4, None) == 3           # K % 128
+    assert g(A16, 0, 256, 128, 128, None, None, 0, None) == 0          # no experts: nothing touched
+    assert g(None, 2, 256, 128, 128, A16, A16, 4, None) == 1
+    assert g(A16, 2, 256, 128, 100, A16, A16, 4, None) == 1           # ldw < K
+    assert g(A16, 2, 256, 128, 128, A16, A16, 6, None) == 1           # lds % 4
+    assert g(A16, 2, 256, 128, 128, MIS, A16, 4, None) == 2
+    t = L.fp8_quant_w_128x128_t
+    assert t(A16, 200, 128, 128, A16, A16, 4, None, None, 0, None) == 3   # N % 128 (W^T's K groups)
+    assert t(A16, 256, 200, 200, A16, A16, 4, None, None, 0, None) == 3   # K % 128
+    assert t(A16, 0, 128, 128, None, None, 0, None, None, 0, None) == 0   # empty: nothing touched
+    assert t(A16, 256, 128, 128, None, A16, 4, None, None, 0, None) == 1  # no qT
+    assert t(A16, 256, 384, 384, A16, A16, 2, None, None, 0, None) == 1   # ldsT < K/128
+    assert t(A16, 256, 128, 128, A16, A16, 4, A16, None, 4, None) == 1    # q without s
+    assert t(A16, 256, 128, 128, A16, A16, 4, A16, A16, 1, None) == 1     # lds < N/128
+    assert t(A16, 256, 128, 132, A16, A16, 4, None, None, 0, None) == 2   # ldw % 8
+    assert t(A16, 256, 128, 128, A16, A16, 4, MIS, A16, 4, None) == 2     # q misaligned
+
+
+def test_masked_rejects(L):
+    f = L.fp8_masked_grouped_gemm_blockscaled
+    ok = dict(A=A16, sa=A16, ldsa=128, B=A16, sb=A16, ldsb=4, cnt=A16, E=2, cap=64, C=A16, ldc=256, cdt=0,
+              N=256, K=512, ws=A16, wsb=1 << 26, st=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["A"], a["sa"], a["ldsa"], a["B"], a["sb"], a["ldsb"], a["cnt"], a["E"], a["cap"], a["C"],
+                 a["ldc"], a["cdt"], a["N"], a["K"], a["ws"], a["wsb"], a["st"])
+
+    assert call(E=0, A=None, cnt=None) == 0      # no experts: nothing touched
+    assert call(E=-1) == 1
+    assert call(cnt=None) == 1
+    assert call(cdt=2) == 1
+    assert call(cap=72) == 3                     # cap % 16
+    assert call(cap=272, ldsa=544) == 3          # cap > 256
+    assert call(N=250, ldc=256) == 3             # N % 16
+    assert call(ldsa=100) == 1                   # ldsa < E * cap
+    assert call(ldsb=1, N=256) == 1              # ldsb < ceil(N/128)... and % 4
+    assert call(ldc=200) == 1
+    assert call(cnt=ctypes.c_void_p(0x10002)) == 2   # counts not 4-byte aligned
+    assert call(ws=ctypes.c_void_p(0x10010)) == 2    # workspace not 256-byte aligned
+    need = L.fgf8_masked_gemm_workspace_bytes(2, 64, 256, 512)
+    assert need > 256                            # 2 experts x 2 weight tiles: split-K partials
+    assert call(wsb=need - 1) == 5
+
+
+def test_bf16a_rejects(L):
+    f = L.fp8_gemm_bf16a_blockscaled
+    ok = dict(x=A16, ldx=512, B=A16, sb=A16, ldsb=4, C=A16, ldc=256, cdt=0, M=16, N=256, K=512,
+              ws=A16, wsb=1 << 26, st=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["ldx"], a["B"], a["sb"], a["ldsb"], a["C"], a["ldc"], a["cdt"], a["M"], a["N"],
+                 a["K"], a["ws"], a["wsb"], a["st"])
+
+    assert call(M=0, x=None) == 0                # empty output: nothing touched
+    assert call(x=None) == 1
+    assert call(M=65) == 3                       # at most 64 tokens
+    assert call(K=200, ldx=200) == 3
+    assert call(N=250, ldc=256) == 3
+    assert call(ldx=256) == 1                    # ldx < K
+    assert call(ldsb=2) == 1
+    assert call(x=MIS) == 2
+    assert call(ldx=516) == 2                    # BF16 rows must be 16-byte multiples
+    assert call(wsb=16) == 5
+
+
 def test_probe_rejects(L):
     f = L.fgf8_mma_probe
     assert f(A16, A16, A16, 24, 128, A16, None) == 3
