@@ -302,7 +302,7 @@ size_t fgf8_masked_gemm_workspace_bytes(int32_t num_experts, int64_t cap, int64_
 
 /* Workspace size (bytes) with which the GEMM entry points can use every
  * schedule for this shape (for dense GEMMs, the last-wave split, about
- * 19 MiB), and the least they accept (FGF8_ERR_WORKSPACE_TOO_SMALL below it). */
+ * 18.5 MiB), and the least they accept (FGF8_ERR_WORKSPACE_TOO_SMALL below it). */
 size_t fgf8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 size_t fgf8_gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 
