@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "FGF8Error", "lib", "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
     "fp8_gemm_blockscaled",
-    "fp8_grouped_gemm_blockscaled", "fgf8_mma_probe", "fgf8_read_status", "workspace_for",
+    "fp8_grouped_gemm_blockscaled", "fp8_masked_grouped_gemm_blockscaled", "fp8_gemm_bf16a_blockscaled",
+    "fp8_quant_w_128x128_t", "fgf8_mma_probe", "fgf8_read_status", "fgf8_noalloc_read_status", "workspace_for",
     "BSCALE_BLOCK128", "BSCALE_ROW1x128", "OUT_BF16", "OUT_FP32",
 ]
 
@@ -45,7 +46,8 @@ EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_qu
             "fp8_masked_grouped_gemm_blockscaled", "fp8_gemm_bf16a_blockscaled", "fgf8_gemm_workspace_bytes", "fgf8_gemm_workspace_min_bytes",
             "fgf8_masked_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div",
-            "fgf8_testing_gemm_schedule"]
+            "fgf8_testing_gemm_schedule", "fgf8_testing_pair_clusters", "fgf8_testing_set_pair",
+            "fgf8_noalloc_read_status"]
 
 
 class FGF8Error(RuntimeError):
@@ -90,10 +92,16 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_bf16a_blockscaled.argtypes = [P, I64, P, P, I64, P, I64, ctypes.c_int, I64, I64, I64, P, SZ, P]
         L.fgf8_masked_gemm_workspace_bytes.restype = SZ
         L.fgf8_read_status.argtypes = [P, P, ctypes.POINTER(I32)]
+        L.fgf8_noalloc_read_status.argtypes = [P, ctypes.POINTER(I32)]
+        L.fgf8_noalloc_read_status.restype = ctypes.c_int
         L.fgf8_mma_probe.argtypes = [P, P, P, I32, I32, P, P]
         L.fgf8_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
         L.fgf8_selftest_scaled_div.argtypes = [P, P, I64, P, P, P]
         L.fgf8_testing_gemm_schedule.argtypes = [I64, I64, I64, I32, SZ, I32, P]
+        L.fgf8_testing_pair_clusters.argtypes = []
+        L.fgf8_testing_pair_clusters.restype = I32
+        L.fgf8_testing_set_pair.argtypes = [I32]
+        L.fgf8_testing_set_pair.restype = ctypes.c_int
         for name in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_grouped",
                      "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc",
                      "fp8_grouped_gemm_blockscaled", "fgf8_read_status", "fgf8_mma_probe",
@@ -122,17 +130,36 @@ def round_up(v: int, m: int) -> int:
 
 _workspaces: dict = {}
 
+# Bytes at the start of every GEMM workspace that must be zero when a call
+# starts: the device status word and the split kernels' arrival counters.
+WS_ZEROED_BYTES = 256 + 256 * 4
 
-def workspace_for(device, nbytes: int) -> torch.Tensor:
+
+def workspace_for(device, nbytes: int, stream=None) -> torch.Tensor:
     """A zero-filled, 256-byte aligned device workspace of at least nbytes,
-    cached per device (the kernels leave it zeroed for the next call)."""
+    cached per (device, stream): calls on one stream run in order and may share
+    one (the kernels leave it zeroed for the next call); calls on different
+    streams could overlap and get different ones."""
     device = torch.device(device)
-    ws = _workspaces.get(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    key = (device, stream.cuda_stream)
+    ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
         assert ws.data_ptr() % 256 == 0
-        _workspaces[device] = ws
+        _workspaces[key] = ws
     return ws
+
+
+def _check_device(ws: torch.Tensor, where: str):
+    """Read the workspace's device status (synchronizes the stream).  After an
+    expired device-side wait the kernels may have left arrival counters
+    non-zero: clear them, then raise FGF8Error(FGF8_ERR_TIMEOUT)."""
+    st, site = fgf8_read_status(ws)
+    if st != 0:
+        ws[:WS_ZEROED_BYTES].zero_()
+        raise FGF8Error(st, f"{where} (device wait site {site})")
 
 
 def fp8_quant_act_1x128(x: torch.Tensor, rows: bool = True, transposed: bool = False):
@@ -200,9 +227,11 @@ def fp8_quant_w_128x128_grouped(w: torch.Tensor):
 
 
 def fp8_gemm_blockscaled(A, sa, B, sb, bkind: int = BSCALE_BLOCK128, out_dtype=torch.bfloat16,
-                         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+                         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         check: bool = False):
     """C = A_hat * B_hat^T.  A [M,K] and B [N,K] uint8 E4M3 codes, sa [K/128, ldsa],
-    sb [K/128, ldsb] float32 (block or per-row kind)."""
+    sb [K/128, ldsb] float32 (block or per-row kind).  check=True waits for
+    the GEMM and raises FGF8Error if a device-side wait expired."""
     M, K = A.shape
     N = B.shape[0]
     if out is None:
@@ -214,12 +243,15 @@ def fp8_gemm_blockscaled(A, sa, B, sb, bkind: int = BSCALE_BLOCK128, out_dtype=t
                                     _ptr(out), out.stride(0), cdt, M, N, K, _ptr(ws), ws.numel(),
                                     _stream(A.device))
     _check(st, "fp8_gemm_blockscaled")
+    if check:
+        _check_device(ws, "fp8_gemm_blockscaled")
     return out
 
 
 def fp8_gemm_bf16a_blockscaled(x, B, sb, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
-                               workspace: torch.Tensor | None = None):
-    """C = quant_1x128(x) * B_hat^T with x: BF16 [M, K] (M <= 64) quantized inside the GEMM."""
+                               workspace: torch.Tensor | None = None, check: bool = False):
+    """C = quant_1x128(x) * B_hat^T with x: BF16 [M, K] (M <= 64) quantized inside the GEMM.
+    check=True waits for the GEMM and raises FGF8Error if a device-side wait expired."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     N = B.shape[0]
@@ -231,13 +263,17 @@ def fp8_gemm_bf16a_blockscaled(x, B, sb, out_dtype=torch.bfloat16, out: torch.Te
     st = lib().fp8_gemm_bf16a_blockscaled(_ptr(x), x.stride(0), _ptr(B), _ptr(sb), sb.stride(0), _ptr(out),
                                           out.stride(0), cdt, M, N, K, _ptr(ws), ws.numel(), _stream(x.device))
     _check(st, "fp8_gemm_bf16a_blockscaled")
+    if check:
+        _check_device(ws, "fp8_gemm_bf16a_blockscaled")
     return out
 
 
 def fp8_grouped_gemm_blockscaled(A, sa, B, sb, m_indices, out_dtype=torch.bfloat16,
-                                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+                                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                 check: bool = False):
     """Contiguous-layout grouped GEMM.  A [M_total,K], B [E,N,K], sb [E,K/128,ldsb],
-    m_indices int32 [M_total] (-1 = padding row, left unwritten)."""
+    m_indices int32 [M_total] (-1 = padding row, left unwritten).  check=True
+    waits for the GEMM and raises FGF8Error if a device-side wait expired."""
     M, K = A.shape
     E, N, _ = B.shape
     if out is None:
@@ -249,15 +285,19 @@ def fp8_grouped_gemm_blockscaled(A, sa, B, sb, m_indices, out_dtype=torch.bfloat
                                             _ptr(m_indices), E, _ptr(out), out.stride(0), cdt, M, N, K,
                                             _ptr(ws), ws.numel(), _stream(A.device))
     _check(st, "fp8_grouped_gemm_blockscaled")
+    if check:
+        _check_device(ws, "fp8_grouped_gemm_blockscaled")
     return out
 
 
 def fp8_masked_grouped_gemm_blockscaled(A, sa, B, sb, counts, out_dtype=torch.bfloat16,
-                                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+                                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                        check: bool = False):
     """Masked-layout grouped GEMM (decode MoE).  A [E, cap, K] uint8 with sa [K/128, ldsa]
     (the 1x128 scales of the stacked [E*cap, K] slots), B [E, N, K] with sb [E, K/128, ldsb],
     counts int32 [E] on the device.  Returns C [E, cap, N]; rows past each expert's count
-    are left as they were in `out`."""
+    are left as they were in `out`.  check=True waits for the GEMM and raises
+    FGF8Error if a device-side wait expired."""
     E, cap, K = A.shape
     N = B.shape[1]
     assert sa.dim() == 2 and sa.stride(1) == 1
@@ -272,6 +312,8 @@ def fp8_masked_grouped_gemm_blockscaled(A, sa, B, sb, counts, out_dtype=torch.bf
                                                    _ptr(counts), E, cap, _ptr(out), out.stride(1), cdt, N, K,
                                                    _ptr(ws), ws.numel(), _stream(A.device))
     _check(st, "fp8_masked_grouped_gemm_blockscaled")
+    if check:
+        _check_device(ws, "fp8_masked_grouped_gemm_blockscaled")
     return out
 
 
@@ -291,13 +333,22 @@ def fgf8_testing_gemm_schedule(M: int, N: int, K: int, bkind: int = BSCALE_BLOCK
     ws_bytes defaults to fgf8_gemm_workspace_bytes(M, N, K, 1)."""
     if ws_bytes is None:
         ws_bytes = lib().fgf8_gemm_workspace_bytes(M, N, K, 1)
-    out = (ctypes.c_int32 * 4)()
+    out = (ctypes.c_int32 * 5)()
     _check(lib().fgf8_testing_gemm_schedule(M, N, K, bkind, ws_bytes, num_sms, out), "fgf8_testing_gemm_schedule")
-    return {"small_m": out[0], "bn": out[1], "dp_tiles": out[2], "tail_s": out[3]}
+    return {"small_m": out[0], "bn": out[1], "dp_tiles": out[2], "tail_s": out[3], "pair": out[4]}
 
 
 def fgf8_read_status(workspace: torch.Tensor):
     """(status, site) of the device status word; resets it.  Synchronizes the stream."""
     site = ctypes.c_int32(0)
     st = lib().fgf8_read_status(_ptr(workspace), _stream(workspace.device), ctypes.byref(site))
+    return st, site.value
+
+
+def fgf8_noalloc_read_status(device=None):
+    """(status, site) of the allocation-free GEMM's scratch on the current
+    device; resets it.  Synchronizes the current stream."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    site = ctypes.c_int32(0)
+    st = lib().fgf8_noalloc_read_status(_stream(dev), ctypes.byref(site))
     return st, site.value

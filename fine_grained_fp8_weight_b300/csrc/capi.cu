@@ -20,6 +20,7 @@ struct DeviceInfo {
     int num_sms;
 };
 DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
 
 // Compute capability 10.3 (B300) only: the kernels are built for sm_103a.
 fgf8_status current_device(int *num_sms)
@@ -27,6 +28,7 @@ fgf8_status current_device(int *num_sms)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FGF8_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FGF8_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
     DeviceInfo &d = g_devices[dev];
     if (d.checked == 0) {
         int major = 0, minor = 0, sms = 0;
@@ -73,7 +75,7 @@ const char *fgf8_status_string(fgf8_status st)
 
 const char *fgf8_version(void)
 {
-    return "fgf8 0.7 sm_103a";
+    return "fgf8 0.8 sm_103a";
 }
 
 fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
@@ -156,9 +158,12 @@ size_t fgf8_gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t nu
     return fgf8::gemm_workspace_min_bytes(M, N, K, num_experts);
 }
 
+// Host checks of a GEMM call; the workspace size is checked only when
+// `check_ws_size` (the allocation-free entry point checks its own scratch).
 static fgf8_status check_gemm(const uint8_t *A, const float *sa, int64_t ldsa, const uint8_t *B, const float *sb,
                               int64_t ldsb, int bkind, void *C, int64_t ldc, int cdt, int64_t M, int64_t N,
-                              int64_t K, void *workspace, size_t ws_bytes, int32_t num_experts)
+                              int64_t K, void *workspace, size_t ws_bytes, int32_t num_experts,
+                              bool check_ws_size = true)
 {
     if (!A || !sa || !B || !sb || !C || !workspace) return FGF8_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1) return FGF8_ERR_INVALID_ARG;
@@ -174,7 +179,8 @@ static fgf8_status check_gemm(const uint8_t *A, const float *sa, int64_t ldsa, c
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(C, 16) ||
         (ldc * esz) % 16 != 0 || !aligned(workspace, 256))
         return FGF8_ERR_MISALIGNED;
-    if (ws_bytes < fgf8::gemm_workspace_min_bytes(M, N, K, num_experts)) return FGF8_ERR_WORKSPACE_TOO_SMALL;
+    if (check_ws_size && ws_bytes < fgf8::gemm_workspace_min_bytes(M, N, K, num_experts))
+        return FGF8_ERR_WORKSPACE_TOO_SMALL;
     return FGF8_OK;
 }
 
@@ -279,14 +285,15 @@ fgf8_status fp8_masked_grouped_gemm_blockscaled(const uint8_t *A, const float *s
 }
 
 // ---------------------------------------------------------------------------
-// Allocation-free GEMM entry point.  Its scratch (the device status word of the
-// GEMM kernel) lives in this file-scope device array instead of a workspace
-// the caller allocates.  Every device that loads the library holds the array
-// until the process exits; all calls on a device share it.
+// Allocation-free GEMM entry point.  Its scratch -- the device status word,
+// the split-K arrival counters and, for the decode-sized GEMMs that split K,
+// their FP32 partial sums -- lives in this file-scope device array instead of
+// a workspace the caller allocates.  Every device that loads the library
+// holds the array until the process exits; all calls on a device share it.
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(1) << 20;        // 1 MiB per device
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;        // 4 MiB per device
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mutex;
@@ -316,22 +323,31 @@ fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int6
                                          int64_t ldc, fgf8_out_dtype cdt, int64_t M, int64_t N, int64_t K,
                                          void *stream)
 {
-    if (M >= 1 && N >= 1 && K >= 1 && fgf8::gemm_workspace_min_bytes(M, N, K, 1) > kStaticScratchBytes)
-        return FGF8_ERR_WORKSPACE_TOO_SMALL;
     int num_sms = 0;
     fgf8_status st = current_device(&num_sms);
     if (st != FGF8_OK) return st;
     void *ws = nullptr;
     st = static_scratch(&ws);
     if (st != FGF8_OK) return st;
-    st = check_gemm(A, sa, ldsa, B, sb, ldsb, bkind, C, ldc, cdt, M, N, K, ws, kStaticScratchBytes, 1);
+    st = check_gemm(A, sa, ldsa, B, sb, ldsb, bkind, C, ldc, cdt, M, N, K, ws, kStaticScratchBytes, 1, false);
     if (st != FGF8_OK) return st;
+    fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, (int)bkind, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M, N, K,
+                     nullptr, 1, ws, kStaticScratchBytes};
+    // the scratch the schedule for this shape really uses (on this device,
+    // with 4 MiB of scratch) must fit
+    if (fgf8::gemm_required_bytes(a, num_sms) > kStaticScratchBytes) return FGF8_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // the previous call's status word (and split-K counters) must not leak into this one
     if (cudaMemsetAsync(ws, 0, fgf8::gemm_workspace_zeroed_bytes(M, N, K, 1), cs) != cudaSuccess) return FGF8_ERR_CUDA;
-    fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, (int)bkind, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M, N, K,
-                     nullptr, 1, ws, kStaticScratchBytes};
     return from_cuda(fgf8::launch_gemm(a, cs, num_sms));
+}
+
+fgf8_status fgf8_noalloc_read_status(void *stream, int32_t *site)
+{
+    void *ws = nullptr;
+    fgf8_status st = static_scratch(&ws);
+    if (st != FGF8_OK) return st;
+    return fgf8_read_status(ws, stream, site);
 }
 
 fgf8_status fgf8_read_status(void *workspace, void *stream, int32_t *site)
@@ -396,7 +412,21 @@ fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t 
     schedule[1] = g.bn;
     schedule[2] = g.dp_tiles;
     schedule[3] = g.tail_s;
+    schedule[4] = g.pair;
     return FGF8_OK;
+}
+
+fgf8_status fgf8_testing_set_pair(int32_t mode)
+{
+    if (mode != 0 && mode != 1) return FGF8_ERR_INVALID_ARG;
+    fgf8::set_pair_mode(mode);
+    return FGF8_OK;
+}
+
+int32_t fgf8_testing_pair_clusters(void)
+{
+    if (current_device(nullptr) != FGF8_OK) return 0;
+    return fgf8::pair_max_clusters();
 }
 
 }  // extern "C"

@@ -14,7 +14,8 @@
 //   - warp 0 (one lane) streams the A/B tiles with TMA into a ring of
 //     shared-memory stages;
 //   - warp 2 copies each K group's scale vectors (sa, and block or per-row
-//     sb) into a separate ring with cp.async, running up to SC groups ahead;
+//     sb) into a separate ring with cp.async, 8 K groups per slot (4 with
+//     per-row B scales) and three slots;
 //   - warp 1 (one lane) issues 4 tcgen05.mma (K = 32 each) per K group into a
 //     fresh FP32 partial in tensor memory, alternating between two TMEM
 //     buffers so that the next group's MMAs run while this one is promoted;
@@ -131,17 +132,20 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a)
     return (v + a - 1) / a * a;
 }
 
-template <int BN, int STAGES, int SC, bool ROW_SB>
+// Scale ring: SS slots of SG K groups each (one barrier handshake per SG
+// groups): per group 128 floats of sa and either the 16-byte chunk holding
+// the tile's 128x128 block scales or BN per-row scales of B.
+template <int BN, int STAGES, int SG, int SS, bool ROW_SB>
 struct Layout {
     static constexpr size_t a_bytes = (size_t)BM * BK;
     static constexpr size_t b_bytes = (size_t)BN * BK;
-    static constexpr int sb_slot = ROW_SB ? BN : 32;         // slot pitch in floats (128-byte aligned slots)
+    static constexpr int sb_pitch = ROW_SB ? BN : 4;         // floats of B scales per K group
     static constexpr size_t off_a = 0;
     static constexpr size_t off_b = off_a + STAGES * a_bytes;
     static constexpr size_t off_sa = off_b + STAGES * b_bytes;
-    static constexpr size_t off_sb = off_sa + (size_t)SC * BM * 4;
-    static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * sb_slot * 4, 16);
-    static constexpr int num_bars = 2 * STAGES + 2 * SC + 4 + 1;
+    static constexpr size_t off_sb = off_sa + (size_t)SS * SG * BM * 4;
+    static constexpr size_t off_bar = align_up(off_sb + (size_t)SS * SG * sb_pitch * 4, 16);
+    static constexpr int num_bars = 2 * STAGES + 2 * SS + 4 + 1;
     static constexpr size_t off_misc = off_bar + (size_t)num_bars * 8;
     static constexpr size_t total = off_misc + 16;
     static constexpr size_t dyn_bytes = total + 1024;    // slack to align the base to 1024
@@ -185,12 +189,12 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, float2 a, float
     *reinterpret_cast<uint4 *>(dst) = o;
 }
 
-template <int BN, int STAGES, int SC, bool ROW_SB, bool OUT_F32>
+template <int BN, int STAGES, int SG, int SS, bool ROW_SB, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const Params p)
 {
-    using L = Layout<BN, STAGES, SC, ROW_SB>;
+    using L = Layout<BN, STAGES, SG, SS, ROW_SB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     uint8_t *sm_a = smem + L::off_a;
@@ -201,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
     uint64_t *sc_full = bars + 2 * STAGES;
-    uint64_t *sc_empty = bars + 2 * STAGES + SC;
-    uint64_t *tm_full = bars + 2 * STAGES + 2 * SC;
+    uint64_t *sc_empty = bars + 2 * STAGES + SS;
+    uint64_t *tm_full = bars + 2 * STAGES + 2 * SS;
     uint64_t *tm_empty = tm_full + 2;
     uint64_t *drain = tm_full + 4;
     uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
@@ -217,13 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < SC; ++i) {
+        for (int i = 0; i < SS; ++i) {
             mbar_init(&sc_full[i], 32);                 // one cp.async arrival per scale-warp lane
             mbar_init(&sc_empty[i], kEpiWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tm_full[i], 1);
-            mbar_init(&tm_empty[i], kEpiWarps);
+            mbar_init(&tm_empty[i], kEpiWarps * 32);    // every promotion thread arrives
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -278,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with 16-byte cp.async copies: generic-proxy writes that do not queue
         // behind the operand tiles in the TMA unit.  Chunks past the end of a
         // scale row are zero-filled without a read.
-        uint32_t it = 0;
+        // Every segment (tile or tail piece) starts a new slot.
+        uint32_t nslot = 0;
         bool ok = true;
         SegIter si;
         int32_t tile, kbeg, kend, piece;
@@ -289,27 +294,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (e < 0) continue;
             const int64_t s_row0 = (int64_t)e * p.sb_rows_per_expert;
             const int64_t sa_x = (int64_t)mb * BM + 4 * lane;
-            for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
-                const uint32_t j = it % SC, phj = (it / SC) & 1;
-                if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+            for (int32_t kb = kbeg; kb < kend; ++kb) {
+                const uint32_t slot = nslot % SS, pos = (uint32_t)(kb - kbeg) % SG;
+                if (pos == 0 && !mbar_wait(&sc_empty[slot], ((nslot / SS) & 1) ^ 1, abort_flag)) {
                     record_timeout(p.status, kSiteProducerScale);
                     ok = false;
                     break;
                 }
-                cp_async_16_zfill(sm_sa + j * BM + 4 * lane, p.sa + (int64_t)kb * p.ldsa + (sa_x < p.ldsa ? sa_x : 0),
+                const uint32_t g = slot * SG + pos;              // K group's place in the ring
+                cp_async_16_zfill(sm_sa + g * BM + 4 * lane, p.sa + (int64_t)kb * p.ldsa + (sa_x < p.ldsa ? sa_x : 0),
                                   sa_x < p.ldsa ? 16u : 0u);
                 const float *sb_row = p.sb + (s_row0 + kb) * p.ldsb;
                 if constexpr (ROW_SB) {
 #pragma unroll
                     for (int h = 0; h < BN / 128; ++h) {
                         const int64_t x = (int64_t)nb * BN + h * 128 + 4 * lane;
-                        cp_async_16_zfill(sm_sb + j * L::sb_slot + h * 128 + 4 * lane, sb_row + (x < p.ldsb ? x : 0),
+                        cp_async_16_zfill(sm_sb + g * L::sb_pitch + h * 128 + 4 * lane, sb_row + (x < p.ldsb ? x : 0),
                                           x < p.ldsb ? 16u : 0u);
                     }
                 } else if (lane == 0) {
-                    cp_async_16_zfill(sm_sb + j * L::sb_slot, sb_row + ((nb * BN / 128) & ~3), 16u);
+                    cp_async_16_zfill(sm_sb + g * L::sb_pitch, sb_row + ((nb * BN / 128) & ~3), 16u);
                 }
-                cp_async_arrive_noinc(&sc_full[j]);
+                if (pos == SG - 1 || kb == kend - 1) {
+                    cp_async_arrive_noinc(&sc_full[slot]);
+                    ++nslot;
+                }
             }
         }
         if (!ok) *abort_flag = 1;
@@ -328,13 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                 const uint32_t buf = it & 1, phb = (it >> 1) & 1;
-                if (!mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
-                    record_timeout(p.status, kSiteMmaTmemEmpty);
+                // The operand stage is normally loaded long before its TMEM
+                // buffer comes free: test it first, so that the buffer's
+                // release is followed directly by the MMAs.
+                if (!mbar_wait(&full[s], ph, abort_flag)) {
+                    record_timeout(p.status, kSiteMmaFull);
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(&full[s], ph, abort_flag)) {
-                    record_timeout(p.status, kSiteMmaFull);
+                if (!mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
+                    record_timeout(p.status, kSiteMmaTmemEmpty);
                     ok = false;
                     break;
                 }
@@ -368,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row = quarter * 32 + lane;
         const uint32_t lane_addr = (quarter * 32) << 16;
         const uint32_t col0 = half * HALF;
-        uint32_t it = 0;
+        uint32_t it = 0;                                    // K groups so far (TMEM buffers)
+        uint32_t nslot = 0;                                 // scale slots so far
         bool ok = true;
         // After a failed wait a warp still walks its remaining segments (without
         // waiting), so that all eight reach the tail's named barrier together.
@@ -383,16 +396,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < HALF / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
             const int sb_sel = ROW_SB ? 0 : ((nb * BN / 128) & 3) + (int)(col0 / 128);
             for (int32_t kb = kbeg; ok && kb < kend; ++kb, ++it) {
-                const uint32_t j = it % SC, phj = (it / SC) & 1;
-                if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
+                const uint32_t slot = nslot % SS, pos = (uint32_t)(kb - kbeg) % SG;
+                if (pos == 0 && !mbar_wait(&sc_full[slot], (nslot / SS) & 1, abort_flag)) {
                     record_timeout(p.status, kSiteEpiScale);
                     ok = false;
                     *abort_flag = 1;
                     break;
                 }
-                const float sa_v = sm_sa[j * BM + row];
-                const float *sbv = sm_sb + j * L::sb_slot + (ROW_SB ? col0 : 0);
-                const float blk = ROW_SB ? 0.0f : sa_v * sm_sb[j * L::sb_slot + sb_sel];
+                const uint32_t g = slot * SG + pos;
+                const float sa_v = sm_sa[g * BM + row];
+                const float *sbv = sm_sb + g * L::sb_pitch + (ROW_SB ? col0 : 0);
+                const float blk = ROW_SB ? 0.0f : sa_v * sm_sb[g * L::sb_pitch + sb_sel];
                 const float2 blk2 = make_float2(blk, blk);
                 const float2 sa2 = make_float2(sa_v, sa_v);
                 const uint32_t buf = it & 1, phb = (it >> 1) & 1;
@@ -432,10 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&tm_empty[buf]);
-                    mbar_arrive(&sc_empty[j]);
+                mbar_arrive(&tm_empty[buf]);
+                if (pos == SG - 1 || kb == kend - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sc_empty[slot]);
+                    ++nslot;
                 }
             }
             if (piece >= 0) {
@@ -1043,16 +1058,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int BN, int STAGES, int SC, bool ROW_SB, bool OUT_F32>
+template <int BN, int STAGES, int SG, int SS, bool ROW_SB, bool OUT_F32>
 cudaError_t launch_variant(const GemmArgs &a, const Params &p, int grid, cudaStream_t stream)
 {
-    using L = Layout<BN, STAGES, SC, ROW_SB>;
+    using L = Layout<BN, STAGES, SG, SS, ROW_SB>;
     CUtensorMap tmA, tmB;
     const int64_t b_rows = a.m_indices ? (int64_t)a.num_experts * a.N : a.N;
     if (!make_tensor_map_2d(&tmA, 1, false, a.A, a.K, a.M, a.K, BK, BM, true) ||
         !make_tensor_map_2d(&tmB, 1, false, a.B, a.K, b_rows, a.K, BK, BN, true))
         return cudaErrorInvalidValue;
-    auto kern = gemm_blockscaled_kernel<BN, STAGES, SC, ROW_SB, OUT_F32>;
+    auto kern = gemm_blockscaled_kernel<BN, STAGES, SG, SS, ROW_SB, OUT_F32>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
     kern<<<grid, kThreads, L::dyn_bytes, stream>>>(tmA, tmB, p);
@@ -1232,11 +1247,13 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
         p.tail_tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
         p.tail_partials = reinterpret_cast<float *>(ws + kWsPartialsOffset);
     }
+    // block scales: slots of 8 K groups; per-row B scales (BN floats per
+    // group): slots of 4
     if (a.bkind == 1)
-        return a.out_f32 ? launch_variant<BN, STAGES, 12, true, true>(a, p, grid, stream)
-                         : launch_variant<BN, STAGES, 12, true, false>(a, p, grid, stream);
-    return a.out_f32 ? launch_variant<BN, STAGES, 12, false, true>(a, p, grid, stream)
-                     : launch_variant<BN, STAGES, 12, false, false>(a, p, grid, stream);
+        return a.out_f32 ? launch_variant<BN, STAGES, 4, 3, true, true>(a, p, grid, stream)
+                         : launch_variant<BN, STAGES, 4, 3, true, false>(a, p, grid, stream);
+    return a.out_f32 ? launch_variant<BN, STAGES, 8, 3, false, true>(a, p, grid, stream)
+                     : launch_variant<BN, STAGES, 8, 3, false, false>(a, p, grid, stream);
 }
 
 template <int NT, int STAGES, bool OUT_F32, bool QX = false>
@@ -1310,11 +1327,35 @@ int choose_bn(const GemmArgs &a, int num_sms)
 
 }  // namespace
 
+// The CTA-pair kernel (gemm_pair.cu) serves dense GEMMs with 128x128 block
+// scales and at least two 128-row blocks only when it has been switched on
+// (fgf8_testing_set_pair): on the B300 it is slower than the 128 x 256
+// single-SM tile on every shape measured, so the planner does not pick it.
+int g_pair_mode = 0;
+
+bool use_pair(const GemmArgs &a)
+{
+    return g_pair_mode != 0 && a.m_indices == nullptr && a.counts == nullptr && a.bkind == 0 && a.M > BM;
+}
+
+void set_pair_mode(int mode)
+{
+    g_pair_mode = mode;
+}
+
 GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
 {
     GemmSchedule g{};
     if (a.m_indices == nullptr && a.bkind == 0 && use_small_m(a.M, a.N, 1, num_sms)) {
         g.small_m = 1;
+        return g;
+    }
+    if (use_pair(a)) {
+        const PairPlan pl = pair_plan(a, num_sms / 2);
+        g.pair = 1;
+        g.bn = pair_tile_n();
+        g.dp_tiles = pl.dp_tiles;
+        g.tail_s = pl.tail_s;
         return g;
     }
     g.bn = choose_bn(a, num_sms);
@@ -1326,11 +1367,29 @@ GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
     return g;
 }
 
+size_t gemm_required_bytes(const GemmArgs &a, int num_sms)
+{
+    const GemmSchedule g = gemm_schedule(a, num_sms);
+    if (g.small_m) {
+        // small-M split-K: the arrival tickets and the FP32 partials of the
+        // split count this device uses (none without a split)
+        const int64_t tiles = (a.N + BM - 1) / BM;
+        const int S = tiles > kMaxCounters ? 1 : small_splits(a.N, a.K, num_sms);
+        return S > 1 ? kWsPartialsOffset + (size_t)tiles * S * small_nt(a.M) * BM * 4 : kWsHeaderBytes;
+    }
+    if (g.tail_s > 1) return g.pair ? pair_tail_workspace_bytes() : tail_workspace_bytes(g.bn);
+    return kWsHeaderBytes;
+}
+
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
     // Few tokens: weights on the MMA's M side, K split across the SMs.
     if (a.m_indices == nullptr && a.bkind == 0 && use_small_m(a.M, a.N, 1, num_sms))
         return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
+    if (use_pair(a)) {
+        const cudaError_t e = launch_pair(a, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (choose_bn(a, num_sms) == 128) return launch_bn<128, 6>(a, stream, num_sms);
     return launch_bn<256, 4>(a, stream, num_sms);
 }

@@ -64,12 +64,34 @@ size_t gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_exp
 // status word and the split-K arrival counters).
 size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 // The schedule launch_gemm picks: small-M kernel, or tile width, whole-tile
-// count and pieces per last-wave tile (1: no split).
+// count and pieces per last-wave tile (1: no split); pair = 1 for the CTA-pair
+// kernel (256 x 256 tiles, bn = 256).
 struct GemmSchedule {
-    int small_m, bn, dp_tiles, tail_s;
+    int small_m, bn, dp_tiles, tail_s, pair;
 };
 GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms);
+// 1: dense block-scaled GEMMs of more than 128 rows run on CTA pairs; 0: the
+// planner's choice (single-SM tiles).  Process-wide, for tests.
+void set_pair_mode(int mode);
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
+// Workspace bytes the schedule launch_gemm picks for `a` (with a.ws_bytes of
+// workspace) reads and writes: the status header, plus the split kernels'
+// counters and partials when it splits.
+size_t gemm_required_bytes(const GemmArgs &a, int num_sms);
+// CTA-pair kernel (gemm_pair.cu): 256 x 256 tiles on two SMs whose tensor
+// cores run as one.  pair_max_clusters() is the number of co-resident pairs on
+// the current device (0: not available); pair_plan the tile count and the
+// last-wave split for `clusters` pairs; launch_pair returns
+// cudaErrorNotSupported when the device cannot run it.
+struct PairPlan {
+    int32_t tiles, dp_tiles, tail_s;
+    int64_t cost;               // K-group steps of the whole schedule on one pair
+};
+int pair_max_clusters();
+int pair_tile_n();          // output columns of a pair tile (128 or 256)
+size_t pair_tail_workspace_bytes();
+PairPlan pair_plan(const GemmArgs &a, int clusters);
+cudaError_t launch_pair(const GemmArgs &a, cudaStream_t stream);
 // Masked grouped layout: scratch size, its zero-initialised prefix, launch.
 size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);
 size_t masked_workspace_zeroed_bytes(int32_t num_experts, int64_t N);

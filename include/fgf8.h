@@ -195,28 +195,43 @@ fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa
  *
  * Same arguments, layouts, checks and result as fp8_gemm_blockscaled, minus
  * the workspace.  It allocates nothing (no cudaMalloc, no cudaFree, no
- * allocating library routine): its scratch is a 1 MiB array in device global
+ * allocating library routine): its scratch is a 4 MiB array in device global
  * memory that every device loading the library holds until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress) with the device current; make that first call
  *     before any stream capture on the device.
- *   - Shapes whose scratch need (fgf8_gemm_workspace_min_bytes(M, N, K, 1))
- *     exceeds 1 MiB are rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any
- *     launch.  The 1 MiB never holds the last-wave split: whole tiles only.
+ *   - The scratch a call needs is that of the schedule it runs on this
+ *     device: 256 bytes, except for decode-sized GEMMs (M <= 256 with at
+ *     most half as many 128-row weight tiles as SMs) that split K, which also
+ *     hold FP32 partials of (weight tiles x splits x M rounded up to 16, 32,
+ *     64, 128 or 256) x 128 x 4 bytes.  A shape that needs more than 4 MiB is
+ *     rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any launch (e.g.
+ *     M = 256, N = 4096, K = 7168; M = 16 with the same N and K fits).  The
+ *     4 MiB never holds the last-wave split of large GEMMs: whole tiles only.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; each call clears the part that must start at zero (the device
- *     status word and, for M <= 256, the split-K arrival counters) on `stream`
- *     before its kernel.  Calls whose work can overlap
- *     on the GPU (different streams, no ordering between them) race on the
- *     array: order them, or use fp8_gemm_blockscaled with separate workspaces.
- *   - A device-side wait that expires leaves its status in the shared array,
- *     which no entry point reads back; the next call clears it.
+ *     status word and the split-K arrival counters) on `stream` before its
+ *     kernel.  Calls whose work can overlap on the GPU (different streams, no
+ *     ordering between them) race on the array: order them, or use
+ *     fp8_gemm_blockscaled with separate workspaces.
+ *   - A device-side wait that expires leaves FGF8_ERR_TIMEOUT in the array's
+ *     status word: fgf8_noalloc_read_status reads it back (and clears it);
+ *     otherwise the next call clears it.
  */
 fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int64_t ldsa,
                                          const uint8_t *B, const float *sb, int64_t ldsb,
                                          fgf8_bscale_kind bkind,
                                          void *C, int64_t ldc, fgf8_out_dtype cdt,
                                          int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * fgf8_noalloc_read_status -- fgf8_read_status for the scratch of
+ * fp8_gemm_blockscaled_noalloc on the current device: synchronizes `stream`,
+ * returns the device status (FGF8_OK or FGF8_ERR_TIMEOUT; the site of the
+ * first expired wait in *site when site != NULL) and clears it.  No
+ * counterpart on the pages.
+ */
+fgf8_status fgf8_noalloc_read_status(void *stream, int32_t *site);
 
 /*
  * fp8_gemm_bf16a_blockscaled -- the block-scaled GEMM with its token operand
@@ -250,9 +265,13 @@ fgf8_status fp8_gemm_bf16a_blockscaled(const void *x, int64_t ldx, const uint8_t
  *   B         : E4M3 [num_experts][N][K] (expert-major, contiguous).
  *   sb        : float [num_experts][K/128][ldsb], 128x128 block scales per
  *               expert, ldsb >= ceil(N/128), ldsb % 4 == 0.
- *   m_indices : int32 [M_total], expert id per row or -1 for a padding row;
- *               all rows of one 128-row block carry the same id (or -1).
- *               Rows of a block whose id is -1 are not written.
+ *   m_indices : int32 [M_total], expert id per row or -1 for a padding row.
+ *               Every 128-row block belongs to one expert: its real rows
+ *               come first and carry that expert's id, any padding rows at
+ *               the end of the expert's group carry -1.  The expert of a
+ *               block is read from its first row; a block whose first row is
+ *               -1 is all padding and is skipped.  Rows marked -1 are not
+ *               written.
  *   C         : [M_total][ldc], as for fp8_gemm_blockscaled.
  *   workspace : at least fgf8_gemm_workspace_bytes(M_total, N, K, num_experts).
  */

@@ -41,15 +41,39 @@ fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, 
  * fp8_gemm_blockscaled picks for a dense M x N x K GEMM with B scales of
  * `bkind` (0 block, 1 per row), a workspace of `ws_bytes` and `num_sms` SMs:
  *   schedule[0] = 1 if the small-M kernel runs (the rest is then 0);
- *   schedule[1] = output tile width (128 or 256 columns, 128 rows);
- *   schedule[2] = tiles computed whole (a multiple of min(num_sms, 148) when
- *                 the last wave is split, else all of them);
- *   schedule[3] = K pieces per remaining tile (1 = no split).
- * `schedule` points to 4 host int32.  Lets tests check the schedule choice on
+ *   schedule[1] = output tile width (128 or 256 columns);
+ *   schedule[2] = tiles computed whole (a multiple of the number of
+ *                 concurrent CTAs, or CTA pairs, when the last wave is
+ *                 split, else all of them);
+ *   schedule[3] = K pieces per remaining tile (1 = no split);
+ *   schedule[4] = 1 if the CTA-pair kernel runs (256 x 256 tiles on two SMs;
+ *                 num_sms / 2 pairs are assumed), 0 for 128-row tiles.
+ * `schedule` points to 5 host int32.  Lets tests check the schedule choice on
  * a CPU and confirm that a GPU case covers the path it is meant to.
  */
 fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t bkind, size_t ws_bytes,
                                        int32_t num_sms, int32_t *schedule);
+
+/*
+ * fgf8_testing_set_pair -- 1: from now on, in this process, dense GEMMs with
+ * 128x128 block scales and more than 128 rows (and more weight tiles than the
+ * small-M kernel takes) run on the CTA-pair kernel: 256 x 128 output tiles on
+ * two SMs whose tensor cores work as one (tcgen05 .cta_group::2), four FP32
+ * partial buffers per SM, even and odd K groups promoted by different warps.
+ * 0: back to the planner's choice (128-row tiles on single SMs, which are
+ * faster on the B300).  Returns FGF8_ERR_INVALID_ARG for other values.  Not
+ * thread-safe: set it while no other thread calls the library.
+ */
+fgf8_status fgf8_testing_set_pair(int32_t mode);
+
+/*
+ * fgf8_testing_pair_clusters -- the number of CTA pairs of the pair GEMM
+ * kernel that the current device runs at once (0 if it cannot run it).
+ * Calls the CUDA runtime's occupancy query; launches nothing.  Passing twice
+ * this number as `num_sms` to fgf8_testing_gemm_schedule gives the schedule
+ * the device actually runs.
+ */
+int32_t fgf8_testing_pair_clusters(void);
 
 #ifdef __cplusplus
 }

@@ -194,23 +194,32 @@ def test_workspace_size(L):
 
 # --- schedule choice (host only) ---
 
-def _tiles(M, N, bn):
-    return -(-M // 128) * -(-N // bn)
+def _tiles(M, N, sch):
+    rows = 256 if sch["pair"] else 128          # a CTA pair covers two 128-row blocks
+    return -(-M // rows) * -(-N // sch["bn"])
 
 
-@pytest.mark.parametrize("sms", [148, 132, 64])
-def test_last_wave_split_invariants(L, sms):
-    """Whole tiles fill whole waves over min(SMs, 148) CTAs; the rest (fewer
-    than that) are cut into s <= K/128 pieces that fit one more wave."""
-    G = min(sms, 148)
+@pytest.fixture
+def pair_on(L):
+    """The CTA-pair kernel switched on for one test (process-wide switch)."""
+    assert L.fgf8_testing_set_pair(1) == 0
+    try:
+        yield
+    finally:
+        assert L.fgf8_testing_set_pair(0) == 0
+
+
+def _check_split_invariants(sms, bkind, pair):
     seen_split = 0
     for M in (257, 384, 1000, 1280, 2560, 4096, 7168):
         for N in (512, 1792, 3072, 4096, 7168, 18432):
             for K in (128, 1024, 2048, 7168, 18432):
-                sch = fg.fgf8_testing_gemm_schedule(M, N, K, 0, num_sms=sms)
+                sch = fg.fgf8_testing_gemm_schedule(M, N, K, bkind, num_sms=sms)
                 if sch["small_m"]:
                     continue
-                tiles = _tiles(M, N, sch["bn"])
+                assert sch["pair"] == pair
+                G = sms // 2 if sch["pair"] else min(sms, 148)
+                tiles = _tiles(M, N, sch)
                 if sch["tail_s"] == 1:
                     assert sch["dp_tiles"] == tiles
                     continue
@@ -220,15 +229,31 @@ def test_last_wave_split_invariants(L, sms):
                 assert 2 <= sch["tail_s"] <= K // 128 and R * sch["tail_s"] <= G
                 # with the least workspace the same GEMM runs whole tiles only
                 wmin = fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1)
-                plain = fg.fgf8_testing_gemm_schedule(M, N, K, 0, ws_bytes=wmin, num_sms=sms)
-                assert plain["tail_s"] == 1 and plain["dp_tiles"] == _tiles(M, N, plain["bn"])
+                plain = fg.fgf8_testing_gemm_schedule(M, N, K, bkind, ws_bytes=wmin, num_sms=sms)
+                assert plain["tail_s"] == 1 and plain["dp_tiles"] == _tiles(M, N, plain)
     assert seen_split > 10
+
+
+@pytest.mark.parametrize("sms", [148, 132, 64])
+@pytest.mark.parametrize("bkind", [0, 1])
+def test_last_wave_split_invariants(L, sms, bkind):
+    """Whole tiles fill whole waves over min(SMs, 148) CTAs; the rest (fewer
+    than that) are cut into s <= K/128 pieces that fit one more wave."""
+    _check_split_invariants(sms, bkind, 0)
+
+
+@pytest.mark.parametrize("sms", [148, 132])
+def test_pair_last_wave_split_invariants(L, pair_on, sms):
+    """The same for the CTA-pair kernel: SMs / 2 pairs, 256 x 128 tiles."""
+    _check_split_invariants(sms, 0, 1)
+    assert fg.fgf8_testing_gemm_schedule(4096, 18432, 7168, 1)["pair"] == 0   # per-row B scales: single SMs
 
 
 def test_schedule_of_the_prefill_pair_and_wgrad(L):
     # 4096 x 7168 x 18432: 896 tiles of 128 x 256 = 6 waves + 8; the 8 run as
     # 8 K pieces each (18 K groups per piece) next to the 6 whole waves
-    assert fg.fgf8_testing_gemm_schedule(4096, 7168, 18432) == {"small_m": 0, "bn": 256, "dp_tiles": 888, "tail_s": 8}
+    assert fg.fgf8_testing_gemm_schedule(4096, 7168, 18432) == {"small_m": 0, "bn": 256, "dp_tiles": 888,
+                                                                "tail_s": 8, "pair": 0}
     # 4096 x 18432 x 7168: 2304 tiles = 15 waves + 84; splitting 84 tiles
     # cannot fill a wave better than whole tiles do
     assert fg.fgf8_testing_gemm_schedule(4096, 18432, 7168)["tail_s"] == 1
@@ -238,8 +263,22 @@ def test_schedule_of_the_prefill_pair_and_wgrad(L):
     assert fg.fgf8_testing_gemm_schedule(16, 4096, 7168)["small_m"] == 1
 
 
+def test_pair_schedule_of_the_prefill_pair(L, pair_on):
+    # 4096 x 18432 x 7168 on 74 pairs: 16 x 144 = 2304 tiles of 256 x 128 = 31
+    # waves + 10; the 10 run as 4 K pieces each
+    assert fg.fgf8_testing_gemm_schedule(4096, 18432, 7168) == {"small_m": 0, "bn": 128, "dp_tiles": 2294,
+                                                                "tail_s": 4, "pair": 1}
+    # one 128-row block: single-SM tiles
+    assert fg.fgf8_testing_gemm_schedule(128, 18432, 7168)["pair"] == 0
+
+
+def test_set_pair_rejects(L):
+    assert L.fgf8_testing_set_pair(2) == 1
+    assert L.fgf8_testing_set_pair(-1) == 1
+
+
 def test_schedule_rejects(L):
-    out = (ctypes.c_int32 * 4)()
+    out = (ctypes.c_int32 * 5)()
     f = L.fgf8_testing_gemm_schedule
     assert f(0, 128, 128, 0, 1 << 20, 148, out) == 1
     assert f(128, 128, 100, 0, 1 << 20, 148, out) == 1

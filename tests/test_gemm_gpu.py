@@ -116,7 +116,7 @@ def _split_case(M, N, K, bkind):
 def test_last_wave_split(M, N, K, bkind, bn, out):
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     sch = fg.fgf8_testing_gemm_schedule(M, N, K, bkind, num_sms=sm)
-    assert sch["bn"] == bn and sch["tail_s"] > 1, sch
+    assert sch["pair"] == 0 and sch["bn"] == bn and sch["tail_s"] > 1, sch
     ops, rows, Cr, S = _split_case(M, N, K, bkind)
     dt = torch.bfloat16 if out == "bf16" else torch.float32
     ws_min = torch.zeros(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), dtype=torch.uint8, device=DEV)
@@ -126,6 +126,76 @@ def test_last_wave_split(M, N, K, bkind, bn, out):
         torch.cuda.synchronize()
         Cg = bf16_out_to_f64(C) if dt == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
         assert_within_bound(Cg[rows], Cr, S, f"{label} {M}x{N}x{K}")
+
+
+# CTA-pair kernel (256 x 128 tiles on two SMs whose tensor cores run as one;
+# off by default, switched on by the test hook): M blocks go in pairs, so the
+# last pair's second CTA may hold a few rows past M or none at all; N may end
+# inside a tile or be narrower than one; one 128-row block past the first
+# (M = 129) with many weight tiles; odd K-group counts (the even and odd
+# promotion warps get different numbers of groups).
+@pytest.fixture
+def pair_on():
+    assert fg.lib().fgf8_testing_set_pair(1) == 0
+    try:
+        yield
+    finally:
+        assert fg.lib().fgf8_testing_set_pair(0) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 256, 128), (384, 272, 512), (129, 18432, 256), (640, 48, 384),
+                                   (1000, 1040, 1152), (2048, 4096, 2048)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_pair_shapes(M, N, K, out, pair_on):
+    assert fg.fgf8_testing_gemm_schedule(M, N, K)["pair"] == 1
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (N, K), 0.02)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    rows = _rows_per_block(M, 4, M + 1) if M * N * K > 2 ** 31 else None
+    Cg, Cr, S = _run_dense(A, B, dt, rows=rows)
+    assert_within_bound(Cg, Cr, S, f"pair {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 2048, 2048), (1280, 4096, 2048), (768, 4096, 2048)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_pair_last_wave_split(M, N, K, out, pair_on):
+    # the planner with the pairs this device runs at once: some tiles are cut
+    # into K pieces; the same GEMM with the least workspace runs whole tiles
+    sm = 2 * fg.lib().fgf8_testing_pair_clusters()
+    sch = fg.fgf8_testing_gemm_schedule(M, N, K, 0, num_sms=sm)
+    assert sch["pair"] == 1 and sch["tail_s"] > 1, sch
+    ops, rows, Cr, S = _split_case(M, N, K, 0)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    ws_min = torch.zeros(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), dtype=torch.uint8, device=DEV)
+    for label, ws in (("split", None), ("whole tiles", ws_min)):
+        C = fg.fp8_gemm_blockscaled(*ops, out_dtype=dt, workspace=ws)
+        torch.cuda.synchronize()
+        Cg = bf16_out_to_f64(C) if dt == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
+        assert_within_bound(Cg[rows], Cr, S, f"pair {label} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,out", [(2048, 4096, 4096, "bf16"), (1280, 4096, 2048, "fp32"),
+                                       (3072, 1792, 2048, "bf16")])
+def test_pair_repeated_launches_bitwise_identical(M, N, K, out, pair_on):
+    _repeat_check(M, N, K, 0, out)
+
+
+def test_pair_output_row_stride_and_untouched_padding(pair_on):
+    # rows past M and columns past N of a larger output buffer stay as they were
+    rng = np.random.default_rng(16)
+    A = wl.bf16_normal(rng, (300, 256))
+    B = wl.bf16_normal(rng, (272, 256), 0.02)
+    qa, sa = oracle.quant_act_1x128(A)
+    qb, sb = oracle.quant_w_128x128(B)
+    big = torch.full((512, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = big[:300, :272]
+    assert fg.fgf8_testing_gemm_schedule(300, 272, 256)["pair"] == 1
+    fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:, 272:]).all() and torch.isnan(big[300:]).all(), "elements past M or N were written"
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb)
+    assert_within_bound(bf16_out_to_f64(out), Cr, S)
 
 
 # M <= 256 takes the small-M path (weights on the MMA's M side, K split over
@@ -230,6 +300,53 @@ def test_grouped_small(counts):
     assert np.all(np.isnan(Cg[~real])), "padding rows were written"
 
 
+# Grouped contiguous layout at full size (32 experts, 32 768 tokens padded to
+# 34 944 rows, N = 4096, K = 7168): both operands quantized on the GPU by the
+# package's quantizers and checked bit for bit against the oracle's codes and
+# scales (every weight byte, every activation row), then the grouped GEMM
+# against the oracle's binary64 result on rows of every expert -- its first
+# and last real rows, two rows between, and the first row after each padding
+# boundary -- with every padding row left unwritten.  At this size each CTA
+# walks ~15 tiles of the m-outer schedule, so expert changes inside one CTA's
+# walk and padding blocks between them are covered.
+def test_full_size_moe_grouped():
+    w = wl.moe_grouped().gemms[0]
+    E, N, K = w.B.shape
+    Mp = w.A.shape[0]
+    A = dev_bf16(w.A)
+    qa, sa, _, _ = fg.fp8_quant_act_1x128(A)
+    del A
+    Bd = wl.bf16_bits_to_torch(w.B).to(DEV)
+    qb, sb = fg.fp8_quant_w_128x128_grouped(Bd)
+    del Bd
+    mi = torch.from_numpy(w.m_indices).to(DEV)
+    out = torch.full((Mp, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    fg.fp8_grouped_gemm_blockscaled(qa, sa, qb, sb, mi, out=out, check=True)
+    torch.cuda.synchronize()
+    rqa, rsa = oracle.quant_act_1x128(w.A)
+    assert np.array_equal(qa.cpu().numpy(), rqa), "activation codes differ from the oracle"
+    assert np.array_equal(sa.cpu().numpy()[:, :Mp].view(np.uint32), rsa[:, :Mp].view(np.uint32))
+    qbh, sbh = qb.cpu().numpy(), sb.cpu().numpy()
+    rqb = np.empty_like(qbh)
+    rsb = np.empty_like(sbh)
+    for e in range(E):
+        rqb[e], rsb[e] = oracle.quant_w_128x128(w.B[e])
+        assert np.array_equal(qbh[e], rqb[e]), f"weight codes of expert {e} differ from the oracle"
+        assert np.array_equal(sbh[e, :, :N // 128].view(np.uint32), rsb[e, :, :N // 128].view(np.uint32))
+    starts = np.concatenate([[0], np.cumsum((w.counts + 127) // 128 * 128)[:-1]])
+    rng = np.random.default_rng(31)
+    rows = []
+    for e, (r0, c) in enumerate(zip(starts, w.counts)):
+        if c == 0:
+            continue
+        rows += [r0, r0 + c - 1] + [int(r0 + x) for x in rng.integers(0, c, 2)]
+    rows = np.unique(np.array(rows, np.int64))
+    Cr, S = oracle.grouped_gemm_blockscaled(rqa, rsa, rqb, rsb, w.m_indices, rows=rows)
+    assert_within_bound(bf16_out_to_f64(out[torch.from_numpy(rows).to(DEV)]), Cr, S, "moe grouped")
+    pad = torch.from_numpy(w.m_indices < 0).to(DEV)
+    assert bool(torch.isnan(out[pad]).all()), "padding rows were written"
+
+
 # --- full-size workloads, sampled rows ---
 
 
@@ -272,6 +389,10 @@ def test_full_size_wgrad_sampled():
                                              (64, 7168, 4096, 0, "bf16"), (200, 2048, 4096, 0, "fp32"),
                                              (2560, 4096, 4096, 0, "bf16"), (1280, 4096, 2048, 1, "fp32")])
 def test_repeated_launches_bitwise_identical(M, N, K, bkind, out):
+    _repeat_check(M, N, K, bkind, out)
+
+
+def _repeat_check(M, N, K, bkind, out):
     g = torch.Generator(device="cpu").manual_seed(M + N + K + bkind)
     qa = torch.randint(0, 256, (M, K), dtype=torch.uint8, generator=g)
     qa[(qa & 0x7F) == 0x7F] = 0x3C                  # no NaN codes
@@ -290,6 +411,41 @@ def test_repeated_launches_bitwise_identical(M, N, K, bkind, out):
         bad = (o.view(torch.int16 if dt == torch.bfloat16 else torch.int32)
                != outs[0].view(torch.int16 if dt == torch.bfloat16 else torch.int32))
         assert not bool(bad.any()), f"launch {i} differs at {bad.nonzero()[:4].tolist()}"
+
+
+# The grouped layout repeated: m-outer tile walk with several tiles per CTA,
+# expert changes inside a CTA's walk, padding blocks between experts and an
+# empty expert; the whole output (padding rows left NaN) must match bit for bit.
+@pytest.mark.parametrize("counts,N,K", [([700, 300, 0, 1000, 130, 2000, 50, 640], 4096, 1024),
+                                        ([129, 1, 255, 3000, 77], 2048, 2048)])
+def test_grouped_repeated_launches_bitwise_identical(counts, N, K):
+    g = torch.Generator(device="cpu").manual_seed(sum(counts) + N + K)
+    E = len(counts)
+    padded = [(c + 127) // 128 * 128 for c in counts]
+    Mp = sum(padded)
+    mi = np.full(Mp, -1, np.int32)
+    r = 0
+    for e, (c, pc) in enumerate(zip(counts, padded)):
+        mi[r:r + c] = e
+        r += pc
+    qa = torch.randint(0, 256, (Mp, K), dtype=torch.uint8, generator=g)
+    qa[(qa & 0x7F) == 0x7F] = 0x3C
+    qb = torch.randint(0, 256, (E, N, K), dtype=torch.uint8, generator=g)
+    qb[(qb & 0x7F) == 0x7F] = 0x3C
+    sa = torch.rand((K // 128, Mp), generator=g) + 0.5
+    sb = torch.rand((E, K // 128, ((N + 127) // 128 + 3) // 4 * 4), generator=g) + 0.5
+    args = [t.to(DEV) for t in (qa, sa, qb, sb)] + [torch.from_numpy(mi).to(DEV)]
+    outs = []
+    for _ in range(5):
+        o = torch.full((Mp, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+        fg.fp8_grouped_gemm_blockscaled(*args, out=o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    ref = outs[0].view(torch.int16)
+    for i, o in enumerate(outs[1:], 1):
+        bad = o.view(torch.int16) != ref
+        assert not bool(bad.any()), f"launch {i} differs at {bad.nonzero()[:4].tolist()}"
+    assert bool(torch.isnan(outs[0][torch.from_numpy(mi < 0).to(DEV)]).all())
 
 
 # --- data gradient dX = dY * W: A = dY (1x128 along N), B = W^T (128x128) ---

@@ -3,12 +3,15 @@ callers that may not allocate device memory -- a plugin whose host framework
 owns all GPU memory, or a loop where an allocation could stall.  It keeps its
 scratch in a library-owned device array instead of a caller workspace.
 
-Checked through the C ABI against the workspace entry point
-(fp8_gemm_blockscaled) on two calls in a row with different shapes, output
-types and scale kinds, within the GEMM tolerance used throughout the tests:
-|C_noalloc - C_workspace| <= 2^-7 * sum|a_hat*b_hat| + 1e-6.  This file is
-collected last so that a failure here stops a -x run only after every other
-test has run."""
+Checked through the C ABI on calls in a row with different shapes, output
+types and scale kinds -- large tiles and the decode-size path that splits K
+over the shared scratch, twice in a row so that the scratch's arrival
+counters are reused -- against the oracle's binary64 result within the GEMM
+tolerance used throughout the tests, |C - C_ref| <= 2^-7 * sum|a_hat*b_hat|
++ 1e-6, and against the workspace entry point (fp8_gemm_blockscaled) within
+the same tolerance.  A shape whose scratch would not fit is rejected before
+anything is written.  This file is collected last so that a failure here
+stops a -x run only after every other test has run."""
 import ctypes
 
 import numpy as np
@@ -55,10 +58,17 @@ def _call_workspace(L, qa, sa, qb, sb, bkind, out):
                                   fg._stream(out.device))
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def test_noalloc_matches_oracle_and_workspace_entry_point():
     L = ensure_built()
-    cases = [(1, 128, 256, 512, 0, torch.bfloat16),      # first call on the device: looks up the array
-             (2, 300, 400, 1024, 1, torch.float32)]      # second call: different shape, kind and output
+    cases = [(1, 128, 256, 512, 0, torch.bfloat16),      # first call on the device: looks up the array; splits K
+             (2, 300, 400, 1024, 1, torch.float32),      # large tiles, per-row B scales
+             (3, 128, 512, 2048, 0, torch.float32),      # split K again: the counters left by the first call
+             (3, 128, 512, 2048, 0, torch.float32),      # ... and the same call once more
+             (4, 128, 512, 1024, 1, torch.bfloat16)]     # M <= 256 with per-row B scales: large tiles
     for seed, M, N, K, bkind, dt in cases:
         qa, sa, qb, sb = _case(seed, M, N, K, bkind)
         ref_out = torch.full((M, N), float("nan"), dtype=dt, device=DEV)
@@ -67,11 +77,33 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert _call_workspace(L, dqa, dsa, dqb, dsb, bkind, ref_out) == 0
         assert _call_noalloc(L, dqa, dsa, dqb, dsb, bkind, got_out) == 0
         torch.cuda.synchronize()
-        _, S = oracle.gemm_blockscaled(qa, sa, qb, sb, bkind)
-        ref = ref_out.float().cpu().numpy().astype(np.float64)
-        got = got_out.float().cpu().numpy().astype(np.float64)
+        Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb, bkind)
+        got = _f64(got_out)
+        bound = 2.0 ** -7 * S + 1e-6
         assert np.all(np.isfinite(got)), "the no-allocation call left outputs unwritten"
-        assert np.all(np.abs(got - ref) <= 2.0 ** -7 * S + 1e-6)
+        assert np.all(np.abs(got - Cr) <= bound), f"{M}x{N}x{K}: outside the bound against the oracle"
+        assert np.all(np.abs(got - _f64(ref_out)) <= bound), f"{M}x{N}x{K}: differs from the workspace entry point"
+        assert fg.fgf8_noalloc_read_status() == (0, 0)
+
+
+def test_noalloc_decode_shape_fits_and_oversized_shape_is_rejected():
+    L = ensure_built()
+    # M = 16, N = 4096, K = 7168 splits K over the SMs: its partials fit the scratch
+    qa, sa, qb, sb = _case(5, 16, 4096, 7168, 0)
+    out = torch.full((16, 4096), float("nan"), dtype=torch.bfloat16, device=DEV)
+    assert _call_noalloc(L, _d(qa), _d(sa), _d(qb), _d(sb), 0, out) == 0
+    torch.cuda.synchronize()
+    rows = np.array([0, 7, 15])
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb, 0, rows=rows)
+    assert np.all(np.abs(_f64(out)[rows] - Cr) <= 2.0 ** -7 * S + 1e-6)
+    # M = 256 with the same weights would need 16 MiB of partials: rejected
+    # before any launch, the output untouched
+    qa2 = torch.zeros((256, 7168), dtype=torch.uint8, device=DEV)
+    sa2 = torch.ones((56, 256), dtype=torch.float32, device=DEV)
+    big = torch.full((256, 4096), float("nan"), dtype=torch.bfloat16, device=DEV)
+    assert _call_noalloc(L, qa2, sa2, _d(qb), _d(sb), 0, big) == 5     # FGF8_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert torch.isnan(big).all(), "a rejected call wrote its output"
 
 
 def test_noalloc_rejects_bad_arguments_without_launching():
