@@ -37,12 +37,21 @@ import numpy as np  # noqa: E402
 
 METRIC = "block-scaled FP8 GEMM TFLOP/s (% of FP8 peak); quantize GB/s (% of HBM)"
 FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
+FUSED_A_MAX_M = 64          # token count up to which fp8_gemm_bf16a_blockscaled takes BF16 tokens
 
 # DRAM bytes (read + write) of one launch, from an ncu capture of that exact
 # kernel build (profiles/ holds the summaries).  Keyed by the library version
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
+    "fgf8 0.9 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_traffic.md
+        "prefill_pair_4096x18432x7168/up.gemm": 166803456 + 126609152,
+        "prefill_pair_4096x18432x7168/down.gemm": 521767168 + 51166720,
+    },
+    "fgf8 0.8 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_traffic.md
+        "prefill_pair_4096x18432x7168/up.gemm": 166761216 + 127433216,
+        "prefill_pair_4096x18432x7168/down.gemm": 625504256 + 51429632,
+    },
     # captured on 0.5; 0.6 changed only the E4M3 encode step (quantizers and the in-GEMM token
     # quantizer), not gemm_blockscaled_kernel
     "fgf8 0.6 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_up.md
@@ -65,61 +74,107 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock, power and clock-event reasons of the GPU, sampled through the
+    driver's NVML library (ctypes) in a background thread every millisecond
+    while the timed region runs, so that a region of a few tens of
+    milliseconds still gets samples; read-only queries, no setting of the GPU
+    is touched.  Falls back to nvidia-smi polling when NVML cannot be loaded."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_s: float = 0.001):
         self.index = index
+        self.period = period_s
+        self.samples = []          # (sm_mhz, power_w, reason bits)
+        self.sm_max = None
+        self._stop = threading.Event()
+        self.thread = None
+        self.nvml = None
         self.proc = None
         self.lines = []
+        self.nvml_error = None
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")      # the driver's NVML, read-only queries only
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            self.nvml = nv
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+            NVML_CLOCK_SM = 1
+            mx, sm, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            if nv.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.sm_max = float(mx.value)
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+            def loop():
+                while not self._stop.is_set():
+                    if (nv.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(sm)) == 0 and
+                            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 and
+                            reasons(h, ctypes.byref(rs)) == 0):
+                        self.samples.append((float(sm.value), pw.value / 1000.0, int(rs.value)))
+                    time.sleep(self.period)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
             self.thread.start()
             t = time.time()
-            while not self.lines and time.time() - t < 5.0:     # first sample before timing starts
-                time.sleep(0.02)
-            self.lines.clear()
+            while not self.samples and time.time() - t < 2.0:     # running before timing starts
+                time.sleep(0.001)
+            self.samples.clear()
+        except Exception as e:  # noqa: BLE001
+            self.nvml = None
+            self.nvml_error = f"{type(e).__name__}: {e}"[:200]
+            self._start_smi()
+
+    def _start_smi(self):
+        fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=lambda: [self.lines.append(l.strip()) for l in self.proc.stdout],
+                                           daemon=True)
+            self.thread.start()
         except OSError:
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, mx, reasons, power = [], None, set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
+        if self.nvml is not None:
+            self._stop.set()
+            self.thread.join(timeout=2.0)
+            self.nvml.nvmlShutdown()
+        elif self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-                power.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = {v: k for k, v in self.REASONS.items()}
+            for line in self.lines:
+                parts = [x.strip() for x in line.split(",")]
+                try:
+                    self.sm_max = float(parts[1])
+                    rs = sum(bits[n] for n, v in zip(names, parts[3:7]) if v.lower() == "active")
+                    self.samples.append((float(parts[0]), float(parts[2]), rs))
+                except (ValueError, IndexError):
+                    continue
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"], "samples": 0}
+        sm = [x[0] for x in self.samples]
+        reasons = sorted({name for _, _, rs in self.samples for bit, name in self.REASONS.items() if rs & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.sm_max, "reasons": reasons,
+                "samples": len(sm), "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": round(max(x[1] for x in self.samples), 1) if self.samples else None,
+                "source": "nvml" if self.nvml is not None else f"nvidia-smi ({self.nvml_error})"}
 
 
 # --------------------------------------------------------------- workloads --
@@ -212,18 +267,28 @@ class DevicePath:
         from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Masked, Wgrad
         self.fg, self.torch, self.dev = fg, torch, dev
         self.ops = []          # (kind, name, callable, bytes or flops)
+        self.workspaces = []   # GEMM workspaces allocated here (the rest are the library's cached ones)
+        self.kernel_of = {}    # GEMM op name -> the kernel that runs it
 
         def gemm_ws(M, N, K):
             # None: the library's recommended workspace (every schedule); else a
             # workspace of the least accepted size (whole output tiles only)
             if not least_workspace:
                 return None
-            return torch.zeros(max(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), 4096), dtype=torch.uint8,
-                               device=dev)
+            ws = torch.zeros(max(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), 4096), dtype=torch.uint8,
+                             device=dev)
+            self.workspaces.append(ws)
+            return ws
+
+        def dense_kernel(M, N, K, bkind=0):
+            sch = fg.fgf8_testing_gemm_schedule(M, N, K, bkind)
+            return "gemm_smallm_kernel" if sch["small_m"] else "gemm_blockscaled_kernel"
 
         self.inputs = []       # (host numpy bits, device tensor) for the end-to-end leg
         self.outputs = []
+        self.groups = []       # per GEMM: (its input indices, its op indices, its output index)
         for g in work.gemms:
+            n_in, n_ops = len(self.inputs), len(self.ops)
             if isinstance(g, Dense):
                 A = wl.bf16_bits_to_torch(g.A).to(dev)
                 B = wl.bf16_bits_to_torch(g.B).to(dev)
@@ -234,7 +299,8 @@ class DevicePath:
                 C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                 self.outputs.append(C)
                 qbytes = lambda r, c, sc: r * c * 3 + sc * 4
-                if fused_a and M <= 64:
+                self.kernel_of[f"{g.name}.gemm"] = dense_kernel(M, N, K)
+                if fused_a and M <= FUSED_A_MAX_M:
                     # tokens quantized inside the GEMM: no activation-quantize launch
                     self.ops.append(("quant", f"{g.name}.quant_w_128x128",
                                      lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128(B)),
@@ -243,17 +309,17 @@ class DevicePath:
                                      lambda A=A, st=st, C=C: fg.fp8_gemm_bf16a_blockscaled(A, st["b"][0], st["b"][1],
                                                                                           out=C),
                                      gemm_flops(g)))
-                    continue
-                self.ops.append(("quant", f"{g.name}.quant_act_1x128",
-                                 lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)),
-                                 qbytes(M, K, M * K // 128)))
-                self.ops.append(("quant", f"{g.name}.quant_w_128x128",
-                                 lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128(B)),
-                                 qbytes(N, K, (N // 128 + 1) * K // 128)))
-                self.ops.append(("gemm", f"{g.name}.gemm",
-                                 lambda st=st, C=C, ws=gemm_ws(M, N, K): fg.fp8_gemm_blockscaled(
-                                     st["a"][0], st["a"][1], st["b"][0], st["b"][1], out=C, workspace=ws),
-                                 gemm_flops(g)))
+                else:
+                    self.ops.append(("quant", f"{g.name}.quant_act_1x128",
+                                     lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)),
+                                     qbytes(M, K, M * K // 128)))
+                    self.ops.append(("quant", f"{g.name}.quant_w_128x128",
+                                     lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128(B)),
+                                     qbytes(N, K, (N // 128 + 1) * K // 128)))
+                    self.ops.append(("gemm", f"{g.name}.gemm",
+                                     lambda st=st, C=C, ws=gemm_ws(M, N, K): fg.fp8_gemm_blockscaled(
+                                         st["a"][0], st["a"][1], st["b"][0], st["b"][1], out=C, workspace=ws),
+                                     gemm_flops(g)))
             elif isinstance(g, Grouped):
                 A = wl.bf16_bits_to_torch(g.A).to(dev)
                 B = wl.bf16_bits_to_torch(g.B).to(dev)
@@ -268,6 +334,7 @@ class DevicePath:
                                  lambda A=A, st=st: st.update(a=fg.fp8_quant_act_1x128(A)), M * K * 3 + M * K // 32))
                 self.ops.append(("quant", f"{g.name}.quant_w_128x128_grouped",
                                  lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128_grouped(B)), E * N * K * 3))
+                self.kernel_of[f"{g.name}.grouped_gemm"] = "gemm_blockscaled_kernel (grouped)"
                 self.ops.append(("gemm", f"{g.name}.grouped_gemm",
                                  lambda st=st, C=C, mi=mi: fg.fp8_grouped_gemm_blockscaled(
                                      st["a"][0], st["a"][1], st["b"][0], st["b"][1], mi, out=C),
@@ -287,6 +354,7 @@ class DevicePath:
                                  E * cap * K * 3 + E * cap * K // 32))
                 self.ops.append(("quant", f"{g.name}.quant_w_128x128_grouped",
                                  lambda B=B, st=st: st.update(b=fg.fp8_quant_w_128x128_grouped(B)), E * N * K * 3))
+                self.kernel_of[f"{g.name}.gemm"] = "gemm_smallm_kernel (masked)"
                 self.ops.append(("gemm", f"{g.name}.gemm",
                                  lambda st=st, C=C, cnt=cnt, E=E, cap=cap, K=K: fg.fp8_masked_grouped_gemm_blockscaled(
                                      st["a"][0].view(E, cap, K), st["a"][1], st["b"][0], st["b"][1], cnt, out=C),
@@ -306,6 +374,7 @@ class DevicePath:
                 self.ops.append(("quant", f"{g.name}.quant_wT_128x128",
                                  lambda W=W, st=st: st.update(b=fg.fp8_quant_w_128x128_t(W)),
                                  N * K * 3 + (N // 128) * (K // 128) * 4))
+                self.kernel_of[f"{g.name}.gemm"] = dense_kernel(T, K, N)
                 self.ops.append(("gemm", f"{g.name}.gemm",
                                  lambda st=st, C=C, ws=gemm_ws(T, K, N): fg.fp8_gemm_blockscaled(
                                      st["a"][0], st["a"][1], st["b"][0], st["b"][1], out=C, workspace=ws),
@@ -325,11 +394,14 @@ class DevicePath:
                 self.ops.append(("quant", f"{g.name}.quant_X_128x1",
                                  lambda X=X, st=st: st.update(b=fg.fp8_quant_act_1x128(X, rows=False, transposed=True)),
                                  T * K * 3 + T * K // 32))
+                self.kernel_of[f"{g.name}.gemm"] = "gemm_blockscaled_kernel (per-row B scales)"
                 self.ops.append(("gemm", f"{g.name}.gemm",
                                  lambda st=st, C=C, ws=gemm_ws(N, K, T): fg.fp8_gemm_blockscaled(
                                      st["a"][2], st["a"][3], st["b"][2], st["b"][3], bkind=fg.BSCALE_ROW1x128,
                                      out=C, workspace=ws),
                                  gemm_flops(g)))
+            self.groups.append((list(range(n_in, len(self.inputs))), list(range(n_ops, len(self.ops))),
+                                len(self.outputs) - 1))
         self.gemm_flops = sum(w for k, _, _, w in self.ops if k == "gemm")
         self.gemm_bytes = {f"{g.name}.{'grouped_gemm' if isinstance(g, Grouped) else 'gemm'}": gemm_bytes(g)
                            for g in work.gemms}
@@ -397,15 +469,59 @@ def run_device(args, rank, world, local_rank):
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     ms_step = ms_total / args.steps
 
-    # Per-kernel device time: each op captured alone and replayed, one event
-    # pair per replay, with an untimed write of a buffer larger than L2 in
-    # between so that no op reads inputs left in L2 by its previous replay.
-    # A short device-side sleep before the first event keeps the GPU busy
-    # while the host submits the event and the replay, so the interval holds
-    # the op alone and not the host's submission latency.
+    per_op = time_ops(path, dev, stream, max(3, min(args.op_reps, args.steps)), fp8_peak, peaks)
+    n_ops = len(path.ops)
+    value = job_tflops(path.gemm_flops, world, ms_step)
+    version = fg.lib().fgf8_version().decode()
+    roof = roofline_of(path, per_op, work.name, fp8_peak, peaks, version)
+    q_bytes = sum(w for k, _, _, w in path.ops if k == "quant")
+    q_ms = sum(e["ms"] for e in per_op.values() if e["kind"] == "quant")
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded numpy normals, bf16)",
+        "config": {"workload": work.name,
+                   "gemms": [n for k, n, _, _ in path.ops if k == "gemm"],
+                   "l2": "no flush: each step reads inputs larger than the 126 MB L2",
+                   "gemm_workspace": args.workspace,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "peak_hbm_gbs": peaks["hbm_gbs"],
+                     "frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "kernels": per_op,
+        "clocks": clk,
+        "gpu_launches": n_ops * args.steps,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(path, args, torch)
+    problems = device_status(fg, path)
+    del path
+    if rank == 0 and not args.no_workloads:
+        result["workloads"] = run_workloads(args, dev, stream, fp8_peak, peaks, version)
+        problems += device_status(fg, None)
+    if problems:
+        # a device-side wait expired somewhere: the kernels that gave up ran
+        # short, so no throughput of this run is reported
+        result["value"] = None
+        result["error"] = "device-side wait expired: " + "; ".join(problems)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(work, args)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+def time_ops(path, dev, stream, reps, fp8_peak, peaks):
+    """Per-kernel device time: each op captured alone into a CUDA graph and
+    replayed, one event pair per replay, with an untimed write of a buffer
+    larger than L2 in between so that no op reads inputs left in L2 by its
+    previous replay.  A short device-side sleep before the first event keeps
+    the GPU busy while the host submits the event and the replay, so the
+    interval holds the op alone and not the host's submission latency."""
+    import torch
     flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
     per_op = {}
-    reps = max(3, min(args.op_reps, args.steps))
     for kind, name, fn, work_units in path.ops:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
@@ -428,83 +544,187 @@ def run_device(args, rank, world, local_rank):
         if kind == "gemm":
             entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
             entry["frac_fp8_peak"] = round(entry["TFLOP/s"] / fp8_peak, 4)
+            entry["GB/s"] = round(path.gemm_bytes[name] / (avg * 1e-3) / 1e9, 1)
+            entry["frac_hbm"] = round(entry["GB/s"] / peaks["hbm_gbs"], 4)
         else:
             entry["GB/s"] = round(work_units / (avg * 1e-3) / 1e9, 1)
             entry["frac_hbm"] = round(entry["GB/s"] / peaks["hbm_gbs"], 4)
         per_op[name] = entry
-    n_ops = len(path.ops)
+    return per_op
 
-    value = job_tflops(path.gemm_flops, world, ms_step)
-    # roofline of the dominant kernel: the GEMM launch that takes longest
+
+def time_ops_rotating(paths, dev, stream, reps, fp8_peak, peaks):
+    """Per-kernel device time for workloads whose operands fit in L2: the
+    same op of len(paths) independent copies of the workload (their operand
+    sets together larger than twice the 126 MB L2) captured back to back into
+    one CUDA graph, so that no launch finds its inputs in L2 and the launch
+    overhead of one graph replay is spread over len(paths) kernels; the L2 is
+    flushed before each timed replay.  Reports the mean time per launch."""
+    import torch
+    flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
+    R = len(paths)
+    per_op = {}
+    for j, (kind, name, _, work_units) in enumerate(paths[0].ops):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for pth in paths:
+                pth.ops[j][2]()
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                for pth in paths:
+                    pth.ops[j][2]()
+        torch.cuda.current_stream(dev).wait_stream(stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        g.replay()
+        for e0, e1 in ev:
+            flush.fill_(1.0)
+            torch.cuda._sleep(200_000)
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize(dev)
+        avg = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps / R
+        entry = {"kind": kind, "ms": round(avg, 5), "timing": f"{R} back-to-back launches on separate operand copies"}
+        if kind == "gemm":
+            entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
+            entry["frac_fp8_peak"] = round(entry["TFLOP/s"] / fp8_peak, 4)
+            entry["GB/s"] = round(paths[0].gemm_bytes[name] / (avg * 1e-3) / 1e9, 1)
+            entry["frac_hbm"] = round(entry["GB/s"] / peaks["hbm_gbs"], 4)
+        else:
+            entry["GB/s"] = round(work_units / (avg * 1e-3) / 1e9, 1)
+            entry["frac_hbm"] = round(entry["GB/s"] / peaks["hbm_gbs"], 4)
+        per_op[name] = entry
+    return per_op
+
+
+def roofline_of(path, per_op, work_name, fp8_peak, peaks, version):
+    """Roofline of the dominant kernel: the GEMM launch that takes longest.
+    Below the ridge point (peak FLOP/s over peak bytes/s) a launch is bound by
+    HBM, above it by the FP8 tensor rate."""
     gemm_ops = [(per_op[name]["ms"], name, w) for kind, name, _, w in path.ops if kind == "gemm"]
     dom_ms, dom_name, dom_flops = max(gemm_ops)
-    gemm_ach = dom_flops / (dom_ms * 1e-3) / 1e12
     dom_bytes = path.gemm_bytes[dom_name]
-    # below the ridge point (peak FLOP/s over peak bytes/s) the launch is bound by HBM
     hbm_bound = dom_flops / dom_bytes < fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    for kind, name, _, w in path.ops:
-        if kind == "gemm":
-            per_op[name]["GB/s"] = round(path.gemm_bytes[name] / (per_op[name]["ms"] * 1e-3) / 1e9, 1)
-            per_op[name]["frac_hbm"] = round(per_op[name]["GB/s"] / peaks["hbm_gbs"], 4)
-    version = fg.lib().fgf8_version().decode()
-    traffic = MEASURED_TRAFFIC.get(version, {}).get(f"{work.name}/{dom_name}")
-    q_bytes = sum(w for k, _, _, w in path.ops if k == "quant")
-    q_ms = sum(e["ms"] for e in per_op.values() if e["kind"] == "quant")
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
-        "data": "synthetic (seeded numpy normals, bf16)",
-        "config": {"workload": work.name,
-                   "gemms": [n for k, n, _, _ in path.ops if k == "gemm"],
-                   "l2": "no flush: each step reads inputs larger than the 126 MB L2",
-                   "gemm_workspace": args.workspace,
-                   "parallelism": f"replicas x{world}"},
-        "roofline": ({"bound": "hbm", "achieved": per_op[dom_name]["GB/s"], "peak": peaks["hbm_gbs"],
-                      "unit": "GB/s", "frac": per_op[dom_name]["frac_hbm"], "traffic": traffic,
-                      "kernel": f"{'gemm_smallm_kernel' if hbm_bound else 'gemm_blockscaled_kernel'} "
-                                f"({dom_name}, {version})",
-                      "algorithmic_bytes_per_launch": dom_bytes,
-                      "peak_note": f"{peaks['source']} HBM copy bandwidth"}
-                     if hbm_bound else
-                     {"bound": "tensor", "achieved": round(gemm_ach, 1), "peak": round(fp8_peak, 1),
-                      "unit": "TFLOP/s", "frac": round(gemm_ach / fp8_peak, 4), "traffic": traffic,
-                      "kernel": f"gemm_blockscaled_kernel ({dom_name}, {version})",
-                      "algorithmic_flops_per_launch": dom_flops,
-                      "peak_note": f"fp8 = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
-                                   f"{peaks['bf16_tflops']} TFLOP/s (sustained bf16 {peaks['bf16_tflops_sustained']})"}),
-        "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "peak_hbm_gbs": peaks["hbm_gbs"],
-                     "frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
-        "kernels": per_op,
-        "clocks": clk,
-        "gpu_launches": n_ops * args.steps,
-    }
-    if not args.no_e2e:
-        result["e2e"] = run_e2e(path, args, torch)
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(work, args)
-    if dist is not None:
-        dist.destroy_process_group()
-    return result
+    traffic = MEASURED_TRAFFIC.get(version, {}).get(f"{work_name}/{dom_name}")
+    kernel = path.kernel_of.get(dom_name, "gemm_blockscaled_kernel")
+    if hbm_bound:
+        return {"bound": "hbm", "achieved": per_op[dom_name]["GB/s"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": per_op[dom_name]["frac_hbm"], "traffic": traffic,
+                "kernel": f"{kernel} ({dom_name}, {version})", "algorithmic_bytes_per_launch": dom_bytes,
+                "peak_note": f"{peaks['source']} HBM copy bandwidth"}
+    ach = dom_flops / (dom_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+            "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "traffic": traffic,
+            "kernel": f"{kernel} ({dom_name}, {version})", "algorithmic_flops_per_launch": dom_flops,
+            "peak_note": f"fp8 = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
+                         f"{peaks['bf16_tflops']} TFLOP/s (sustained bf16 {peaks['bf16_tflops_sustained']})"}
+
+
+def device_status(fg, path):
+    """Read (and clear) the device status word of every GEMM workspace the run
+    used: the library's cached workspaces and any the path allocated itself.
+    Returns the problems found (an expired device-side wait), if any."""
+    wss = list(fg._workspaces.values()) + (list(path.workspaces) if path is not None else [])
+    problems = []
+    for ws in wss:
+        st, site = fg.fgf8_read_status(ws)
+        if st != 0:
+            problems.append(f"status {st} at wait site {site}")
+    return problems
+
+
+# Workloads measured in the line's "workloads" key besides the headline one:
+# the other configurations of the path (tiny GEMM, decode GEMMs, grouped MoE,
+# weight gradient) and the data gradient.
+EXTRA_WORKLOADS = ["tiny", "decode", "moe", "wgrad", "dgrad"]
+# Workloads whose GEMMs each take less BF16 input than this (the decode and
+# tiny GEMMs, whose operands would otherwise come from L2) are timed on
+# ROTATE_COPIES copies back to back (time_ops_rotating); 8 copies of the decode
+# workload's operands take ~2.8 GB, far more than twice L2.
+ROTATE_BELOW_BYTES = 126 << 20
+ROTATE_COPIES = 8
+
+
+def run_workloads(args, dev, stream, fp8_peak, peaks, version):
+    """Per-kernel device times, throughput and roofline fractions of every
+    workload in EXTRA_WORKLOADS (and the decode GEMMs with the tokens quantized
+    inside the GEMM, for comparison), each op replayed with an L2 flush in
+    between."""
+    import torch
+    out = {}
+    names = [w for w in EXTRA_WORKLOADS if w != args.workload] + ["decode:fused_a"]
+    if args.moe_decode:
+        names.append("moe_decode")
+    reps = max(3, min(args.op_reps, 20))
+    for name in names:
+        base, _, variant = name.partition(":")
+        work = make_workload(base)
+        path = DevicePath(work, dev, fused_a=variant == "fused_a")
+        with torch.cuda.stream(stream):
+            path.step()
+        torch.cuda.synchronize(dev)
+        footprint = max(sum(path.inputs[i][1].numel() * path.inputs[i][1].element_size() for i in ins)
+                        for ins, _, _ in path.groups)
+        if footprint < ROTATE_BELOW_BYTES:
+            # operands that fit in L2: copies of the workload timed back to back
+            copies = [path] + [DevicePath(work, dev, fused_a=variant == "fused_a") for _ in range(ROTATE_COPIES - 1)]
+            with torch.cuda.stream(stream):
+                for pth in copies[1:]:
+                    pth.step()
+            torch.cuda.synchronize(dev)
+            per_op = time_ops_rotating(copies, dev, stream, reps, fp8_peak, peaks)
+            del copies
+        else:
+            per_op = time_ops(path, dev, stream, reps, fp8_peak, peaks)
+        key = work.name + (" (tokens quantized in the GEMM)" if variant else "")
+        gflop = path.gemm_flops / 1e9
+        ms = sum(e["ms"] for e in per_op.values())
+        out[key] = {"kernels": per_op, "ms_sum_of_kernels": round(ms, 4),
+                    "gemm_GFLOP": round(gflop, 3), "TFLOP/s_over_kernels": round(gflop / ms, 1),
+                    "roofline": roofline_of(path, per_op, work.name, fp8_peak, peaks, version)}
+        del path, work
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(path, args, torch):
     """Same metric through the public API from pinned host memory: every step
     copies its BF16 inputs host->device, runs the path, and reads the outputs
-    back (device->host), all inside the timed region."""
+    back (device->host), all inside the timed region.  The copies run on a
+    second stream: each GEMM's inputs are copied in order and its quantize
+    and GEMM calls wait only for their own inputs, and each output goes back
+    as soon as its GEMM has finished, so the copies of one GEMM overlap the
+    compute of another (and host-to-device with device-to-host)."""
     from fine_grained_fp8_weight_b300 import workloads as wl
+    dev = path.dev
     host_in = [wl.bf16_bits_to_torch(bits).pin_memory() for bits, _ in path.inputs]
     host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in path.outputs]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    main = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(device=dev)
 
     def e2e_step():
-        for h, (_, d) in zip(host_in, path.inputs):
-            d.copy_(h, non_blocking=True)
-        path.step()
-        for h, d in zip(host_out, path.outputs):
-            h.copy_(d, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        arrived = []
+        with torch.cuda.stream(copy):
+            for ins, _, _ in path.groups:
+                for i in ins:
+                    path.inputs[i][1].copy_(host_in[i], non_blocking=True)
+                arrived.append(torch.cuda.Event())
+                arrived[-1].record(copy)
+        done = []
+        for (ins, ops, _), ev in zip(path.groups, arrived):
+            main.wait_event(ev)
+            for j in ops:
+                path.ops[j][2]()
+            done.append(torch.cuda.Event())
+            done[-1].record(main)
+        with torch.cuda.stream(copy):
+            for (_, _, o), ev in zip(path.groups, done):
+                copy.wait_event(ev)
+                host_out[o].copy_(path.outputs[o], non_blocking=True)
+        copy.synchronize()
+        main.synchronize()
 
     steps = max(1, min(args.steps, 5))
     e2e_step()
@@ -514,70 +734,124 @@ def run_e2e(path, args, torch):
         e2e_step()
     dt = (time.perf_counter() - t) / steps
     return {"value": round(path.gemm_flops / dt / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "inputs copied per GEMM on a second stream, overlapping the other GEMM's compute"}
 
 
-def oracle_sample(work, rows, blocks):
-    """The oracle as it stands (single-threaded plain C) on a bounded sample of
-    each dense GEMM of the workload: `rows` activation rows quantized 1x128,
-    `blocks` 128-row blocks of the weight quantized 128x128, and the
-    rows x (128*blocks) block of the output in binary64.  Returns
-    (GEMM FLOPs of the sample, seconds)."""
+def _quant_slices(pool, fn, x, threads, axis):
+    """fn over slices of x along `axis` (multiples of 128 rows or columns), in
+    parallel; returns the list of (codes, scales) per slice and the slices."""
+    n = x.shape[axis]
+    step = 128 * max(1, (n // 128) // (4 * threads))
+    cuts = [(c, min(n, c + step)) for c in range(0, n, step)]
+    take = (lambda c: np.ascontiguousarray(x[c[0]:c[1]])) if axis == 0 else (
+        lambda c: np.ascontiguousarray(x[:, c[0]:c[1]]))
+    return list(pool.map(lambda c: fn(take(c)), cuts)), cuts
+
+
+def oracle_sample(work, rows, threads, seed=0):
+    """The oracle as it stands (plain C in binary64, called through ctypes,
+    which releases the GIL, so `threads` host threads run it side by side) on
+    each dense GEMM of the workload: every operand of the step quantized in
+    full (A 1x128, B 128x128, in slices of 128 rows or columns spread over the
+    threads), and `rows` seeded rows of the output against all N columns (the
+    rows split over the threads).  Returns (GEMM FLOPs of the sample, measured
+    seconds, seconds of the whole step extrapolated from it: the GEMM part
+    scaled by M / rows)."""
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad
-    flops = 0.0
-    t = time.perf_counter()
-    for g in work.gemms:
-        if isinstance(g, Dgrad):
-            N, K = g.W.shape
-            kb = min(blocks, K // 128)
-            qa, sa = oracle.quant_act_1x128(np.ascontiguousarray(g.dY[:rows]))
-            qb, sb = oracle.quant_w_128x128_t(np.ascontiguousarray(g.W[:, :kb * 128]))
-            oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
-            flops += 2.0 * qa.shape[0] * qb.shape[0] * N
-            continue
-        if not isinstance(g, Dense):
-            continue
-        N, K = g.B.shape
-        nb = min(blocks, (N + 127) // 128)
-        qa, sa = oracle.quant_act_1x128(np.ascontiguousarray(g.A[:rows]))
-        qb, sb = oracle.quant_w_128x128(np.ascontiguousarray(g.B[:nb * 128]))
-        oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
-        flops += 2.0 * qa.shape[0] * qb.shape[0] * K
-    return flops, time.perf_counter() - t
+    oracle.lib()                                 # built and loaded before the threads start
+    flops = secs = full = 0.0
+    rng = np.random.default_rng(seed)
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        for g in work.gemms:
+            if isinstance(g, Dense):
+                A, Bw = g.A, g.B
+            elif isinstance(g, Dgrad):
+                A, Bw = g.dY, g.W
+            else:
+                continue
+            M, K = A.shape
+            t0 = time.perf_counter()
+            parts, cuts = _quant_slices(pool, oracle.quant_act_1x128, A, threads, 0)
+            qa = np.concatenate([q for q, _ in parts])
+            sa = np.zeros((K // 128, (M + 3) // 4 * 4), np.float32)
+            for (r0, r1), (_, s_) in zip(cuts, parts):
+                sa[:, r0:r1] = s_[:, :r1 - r0]
+            if isinstance(g, Dense):
+                N = Bw.shape[0]
+                parts, cuts = _quant_slices(pool, oracle.quant_w_128x128, Bw, threads, 0)
+                sb = np.zeros((K // 128, ((N + 127) // 128 + 3) // 4 * 4), np.float32)
+                for (b0, b1), (_, s_) in zip(cuts, parts):
+                    sb[:, b0 // 128:(b1 + 127) // 128] = s_[:, :(b1 - b0 + 127) // 128]
+            else:                                # B = W^T: slices of W's columns are rows of W^T
+                N = Bw.shape[1]
+                parts, cuts = _quant_slices(pool, oracle.quant_w_128x128_t, Bw, threads, 1)
+                sb = np.zeros((K // 128, (N // 128 + 3) // 4 * 4), np.float32)
+                for (c0, c1), (_, s_) in zip(cuts, parts):
+                    sb[:, c0 // 128:c1 // 128] = s_[:, :(c1 - c0) // 128]
+            qb = np.concatenate([q for q, _ in parts])
+            t1 = time.perf_counter()
+            r = np.sort(rng.choice(M, size=min(rows, M), replace=False))
+            chunks = [c for c in np.array_split(r, threads) if len(c)]
+            list(pool.map(lambda c: oracle.gemm_blockscaled(qa, sa, qb, sb, 0, rows=c), chunks))
+            t2 = time.perf_counter()
+            flops += 2.0 * len(r) * N * K
+            secs += t2 - t0
+            full += (t1 - t0) + (t2 - t1) * (M / len(r))
+    return flops, secs, full
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def cpu_baseline(work, args):
-    flops, dt = oracle_sample(work, args.cpu_rows, args.cpu_blocks)
-    return {"value": round(flops / dt / 1e12, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 2),
-            "sample": f"per GEMM: {args.cpu_rows} activation rows quantized 1x128, the first {args.cpu_blocks} "
-                      f"128-row weight blocks quantized 128x128, that {args.cpu_rows} x {128 * args.cpu_blocks} "
-                      f"output block in binary64 (single-threaded C oracle)"}
+    """The oracle on the host cores: the reference arm's per-step sample
+    (every operand of the step quantized in full, args.cpu_rows seeded rows of
+    each GEMM against all N) run args.cpu_reps times with different rows."""
+    threads = _cores()
+    flops = dt = full = 0.0
+    for rep in range(args.cpu_reps):
+        f, d, fu = oracle_sample(work, args.cpu_rows, threads, seed=rep)
+        flops, dt, full = flops + f, dt + d, full + fu
+    return {"value": round(flops / dt / 1e12, 9), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2), "full_step_seconds_extrapolated": round(full / args.cpu_reps, 1),
+            "sample": f"{args.cpu_reps} x (every operand of the step quantized in full -- A 1x128, B 128x128 -- and "
+                      f"{args.cpu_rows} seeded rows of each GEMM's output against all N in binary64); plain C "
+                      f"oracle on {threads} host threads; the full step's time is extrapolated from it "
+                      f"(GEMM part x M/rows)"}
 
 
 def run_reference(args, rank, world):
     """The reference arm is the oracle, run on the host cores on a bounded
-    sample of the same workload each step (8 rows x one 128-row weight block
-    per GEMM); rank 0 alone runs it."""
+    sample of the same workload each step, the sample cpu_baseline repeats
+    (every operand of the step quantized in full, args.cpu_rows seeded rows of
+    each GEMM against all N); rank 0 alone runs it."""
     if rank != 0:
         return None
     work = make_workload(args.workload)
-    for _ in range(args.warmup):
-        oracle_sample(work, 8, 1)
+    threads = _cores()
+    for i in range(args.warmup):
+        oracle_sample(work, args.cpu_rows, threads, seed=1000 + i)
     flops = secs = 0.0
-    for _ in range(args.steps):
-        f, dt = oracle_sample(work, 8, 1)
+    for i in range(args.steps):
+        f, dt, _ = oracle_sample(work, args.cpu_rows, threads, seed=i)
         flops += f
         secs += dt
     value = flops / secs / 1e12
+    sample = (f"per step: every operand of the step quantized in full (A 1x128, B 128x128) and {args.cpu_rows} "
+              f"seeded rows of each GEMM's output against all N in binary64 (plain C oracle, {threads} host threads)")
     return {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy normals, bf16)",
-            "config": {"workload": work.name, "parallelism": "host oracle, 1 thread"}, "impl": "reference",
-            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                             "sample": "per step and GEMM: 8 activation rows quantized 1x128, one 128-row weight "
-                                       "block quantized 128x128, the 8 x 128 output block in binary64"},
+            "config": {"workload": work.name, "parallelism": f"host oracle, {threads} threads"}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -631,8 +905,10 @@ def main():
                                                                "tiny"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=16)
-    ap.add_argument("--cpu-blocks", type=int, default=16)
+    ap.add_argument("--cpu-rows", type=int, default=4, help="oracle sample: output rows per GEMM")
+    ap.add_argument("--cpu-reps", type=int, default=3, help="oracle baseline: samples (different rows)")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' kernel times")
+    ap.add_argument("--moe-decode", action="store_true", help="also time the masked-layout MoE decode GEMM")
     ap.add_argument("--op-reps", type=int, default=20)
     ap.add_argument("--profile-gemm", action="store_true")
     ap.add_argument("--gemm-index", type=int, default=0)

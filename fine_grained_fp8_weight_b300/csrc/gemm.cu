@@ -80,7 +80,8 @@ struct Params {
     int64_t M, N, K;
     int32_t KB;
     int32_t num_m_blocks, num_n_blocks, num_tiles;
-    int32_t m_major;                    // tile order: 1 = m outer, 0 = n outer
+    int32_t m_major;                    // tile order: 1 = m outer, 0 = n outer within bands of M blocks
+    int32_t band;                       // n outer: M blocks per band (all of them when A fits in L2)
     void *C;
     int64_t ldc;
     const int32_t *m_indices;           // grouped layout when non-null
@@ -164,8 +165,14 @@ __device__ __forceinline__ void tile_coords(int32_t tile, const Params &p, int32
         mb = tile / p.num_n_blocks;
         nb = tile - mb * p.num_n_blocks;
     } else {
-        nb = tile / p.num_m_blocks;
-        mb = tile - nb * p.num_m_blocks;
+        // n outer inside a band of p.band M blocks: the band's A panels stay
+        // in L2 while every B column panel streams past them once
+        const int32_t band_tiles = p.band * p.num_n_blocks;
+        const int32_t b = tile / band_tiles;
+        const int32_t r = tile - b * band_tiles;
+        const int32_t h = min(p.band, p.num_m_blocks - b * p.band);
+        nb = r / h;
+        mb = b * p.band + (r - nb * h);
     }
 }
 
@@ -1204,6 +1211,10 @@ size_t gemm_workspace_zeroed_bytes(int64_t, int64_t, int64_t, int32_t)
 
 namespace {
 
+// A panels that a band of the n-outer walk keeps in the 126 MB L2 (with room
+// for the B panels and output passing through).
+constexpr int64_t kBandBytes = 48ll << 20;
+
 template <int BN>
 Params make_params(const GemmArgs &a)
 {
@@ -1216,6 +1227,14 @@ Params make_params(const GemmArgs &a)
     p.num_n_blocks = (int32_t)((a.N + BN - 1) / BN);
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.m_major = a.m_indices != nullptr ? 1 : 0;
+    // Bands of M blocks whose A panels take at most kBandBytes, as even as
+    // possible: the down projection 4096 x 7168 x 18432 (A 75.5 MB) walks two
+    // bands, reading A once and B twice instead of A once per wave.
+    {
+        const int64_t a_bytes = (int64_t)p.num_m_blocks * BM * a.K;
+        const int64_t nbands = (a_bytes + kBandBytes - 1) / kBandBytes;
+        p.band = (int32_t)((p.num_m_blocks + nbands - 1) / nbands);
+    }
     p.C = a.C;
     p.ldc = a.ldc;
     p.m_indices = a.m_indices;
@@ -1304,9 +1323,12 @@ template <bool OUT_F32>
 cudaError_t launch_small_nt(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
     switch (small_nt(a.counts != nullptr ? a.cap : a.M)) {
-    case 16: return launch_small<16, 8, OUT_F32>(a, stream, num_sms);
-    case 32: return launch_small<32, 8, OUT_F32>(a, stream, num_sms);
-    case 64: return launch_small<64, 8, OUT_F32>(a, stream, num_sms);
+    // as many weight stages as fit next to the token tiles (up to ~220 KB):
+    // a decode CTA streams only 8..14 K groups, so nearly all of them are in
+    // flight from the start instead of waiting for refills
+    case 16: return launch_small<16, 12, OUT_F32>(a, stream, num_sms);
+    case 32: return launch_small<32, 11, OUT_F32>(a, stream, num_sms);
+    case 64: return launch_small<64, 9, OUT_F32>(a, stream, num_sms);
     case 128: return launch_small<128, 6, OUT_F32>(a, stream, num_sms);
     default: return launch_small<256, 4, OUT_F32>(a, stream, num_sms);
     }
