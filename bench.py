@@ -37,7 +37,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "block-scaled FP8 GEMM TFLOP/s (% of FP8 peak); quantize GB/s (% of HBM)"
 FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor rate on Blackwell
-FUSED_A_MAX_M = 64          # token count up to which fp8_gemm_bf16a_blockscaled takes BF16 tokens
+FUSED_A_MAX_M = 256         # token count up to which fp8_gemm_bf16a_blockscaled takes BF16 tokens
 
 # DRAM bytes (read + write) of one launch, from an ncu capture of that exact
 # kernel build (profiles/ holds the summaries).  Keyed by the library version
@@ -917,7 +917,7 @@ def main():
                     help="dense GEMM workspace: the recommended size (last-wave split allowed) or the least "
                          "accepted size (whole output tiles only)")
     ap.add_argument("--fused-a", action="store_true",
-                    help="GEMMs with at most 64 tokens quantize their BF16 tokens inside the GEMM")
+                    help="GEMMs with at most 256 tokens quantize their BF16 tokens inside the GEMM")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -250,7 +250,7 @@ def fp8_gemm_blockscaled(A, sa, B, sb, bkind: int = BSCALE_BLOCK128, out_dtype=t
 
 def fp8_gemm_bf16a_blockscaled(x, B, sb, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
                                workspace: torch.Tensor | None = None, check: bool = False):
-    """C = quant_1x128(x) * B_hat^T with x: BF16 [M, K] (M <= 64) quantized inside the GEMM.
+    """C = quant_1x128(x) * B_hat^T with x: BF16 [M, K] (M <= 256) quantized inside the GEMM.
     check=True waits for the GEMM and raises FGF8Error if a device-side wait expired."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape

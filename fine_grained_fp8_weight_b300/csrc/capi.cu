@@ -227,7 +227,7 @@ fgf8_status fp8_gemm_bf16a_blockscaled(const void *x, int64_t ldx, const uint8_t
     if (!x || !B || !sb || !C || !workspace) return FGF8_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 1) return FGF8_ERR_INVALID_ARG;
     if (cdt != FGF8_OUT_BF16 && cdt != FGF8_OUT_FP32) return FGF8_ERR_INVALID_ARG;
-    if (M > 64 || K % 128 != 0 || N % 16 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
+    if (M > 256 || K % 128 != 0 || N % 16 != 0) return FGF8_ERR_UNSUPPORTED_SHAPE;
     if (N > INT32_MAX / 2 || K > INT32_MAX / 2) return FGF8_ERR_UNSUPPORTED_SHAPE;
     if (ldx < K || ldsb < (N + 127) / 128 || ldsb % 4 != 0 || ldc < N) return FGF8_ERR_INVALID_ARG;
     const int64_t esz = cdt == FGF8_OUT_BF16 ? 2 : 4;

@@ -32,7 +32,7 @@
 // gemm_smallm_kernel (decode, M <= 256 tokens): the weight tile takes the
 // MMA's M side and the tokens its N side, K is split over CTAs with an
 // in-order reduction; the same kernel serves the masked grouped layout
-// (per-expert token slots with device-side counts) and, for M <= 64, the
+// (per-expert token slots with device-side counts) and, for M <= 256, the
 // variant that quantizes BF16 tokens inside the kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -570,47 +570,56 @@ struct SmallParams {
     int64_t ldsb;
 };
 
-template <int NT, int STAGES, int SC, bool QX = false>
+// Shared memory of the small-M kernel.  Work goes in batches of GB K groups:
+// one stage holds the weight and token tiles of GB groups (one barrier
+// handshake per batch), one scale slot their scales, one TMEM buffer their GB
+// partials side by side (GB * NT columns).
+template <int NT, int STAGES, int SC, int GB, bool QX = false>
 struct SmallLayout {
-    static constexpr size_t w_bytes = (size_t)BM * BK;        // 16 KB of weights
-    static constexpr size_t x_bytes = (size_t)NT * BK;        // tokens, E4M3 (swizzled, read by the MMA)
-    static constexpr size_t xb_bytes = QX ? (size_t)NT * BK * 2 : 0;   // tokens as BF16 (quantized in the kernel)
+    static constexpr size_t w_group = (size_t)BM * BK;        // 16 KB of weights per K group
+    static constexpr size_t x_group = (size_t)NT * BK;        // tokens, E4M3 (swizzled, read by the MMA)
+    static constexpr size_t xb_group = QX ? (size_t)NT * BK * 2 : 0;   // tokens as BF16 (quantized in the kernel)
+    static constexpr size_t w_bytes = GB * w_group;           // per stage (batch)
+    static constexpr size_t x_bytes = GB * x_group;
+    static constexpr size_t xb_bytes = GB * xb_group;
     static constexpr size_t off_w = 0;
     static constexpr size_t off_x = off_w + STAGES * w_bytes;
     static constexpr size_t off_xb = align_up(off_x + STAGES * x_bytes, 1024);
-    static constexpr int sa_slot = NT < 32 ? 32 : NT;          // floats; 128-byte aligned TMA targets
+    static constexpr size_t sa_slot = align_up((size_t)GB * NT * 4, 128);   // [GB][NT] floats (a TMA box)
+    static constexpr size_t sb_slot = align_up((size_t)GB * 16, 128);       // [GB][4] floats (a TMA box)
     static constexpr size_t off_sa = align_up(off_xb + STAGES * xb_bytes, 1024);
-    static constexpr size_t off_sb = off_sa + (size_t)SC * sa_slot * 4;
-    static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * 32 * 4, 16);
-    // as many TMEM partial buffers as fit (up to 8): the MMA can run ahead of
-    // the promotion by that many K groups
-    static constexpr int nbuf = (512 / NT) < 8 ? (512 / NT) : 8;
+    static constexpr size_t off_sb = off_sa + (size_t)SC * sa_slot;
+    static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * sb_slot, 16);
+    static constexpr int bufcols = GB * NT;                    // TMEM columns of one batch's partials
+    // as many TMEM buffers as fit (up to 8): the MMA runs that many batches ahead
+    static constexpr int nbuf = (512 / bufcols) < 8 ? (512 / bufcols) : 8;
     static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1 + (QX ? STAGES : 0);
     static constexpr size_t off_misc = off_bar + (size_t)num_bars * 8;
     static constexpr size_t total = off_misc + 16;
     static constexpr size_t dyn_bytes = total + 1024;
-    static constexpr uint32_t tmem_cols = nbuf * NT < 32 ? 32 : nbuf * NT;   // power of two
+    static constexpr uint32_t tmem_cols = nbuf * bufcols < 32 ? 32 : nbuf * bufcols;   // power of two
+    static_assert(dyn_bytes <= 227 * 1024, "shared memory");
 };
 
 // QX: the token operand arrives as BF16 and is quantized 1x128 inside the
 // kernel (no E4M3 round trip through HBM): warps 2 and 3 turn each K group's
 // BF16 token tile into the swizzled E4M3 tile the MMA reads and its scales,
 // by the same rule and code as the quantization kernels (e4m3_rule.cuh).
-template <int NT, int STAGES, int SC, bool OUT_F32, bool QX>
+template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_smallm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                        const SmallParams p)
 {
-    using L = SmallLayout<NT, STAGES, SC, QX>;
-    constexpr int COLS = NT / 2;                 // token columns per promotion warp
+    using L = SmallLayout<NT, STAGES, SC, GB, QX>;
+    constexpr int COLS = NT / 2;                 // token columns per promotion warp and K group
     constexpr int CH = COLS < 32 ? COLS : 32;    // columns per TMEM load
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     uint8_t *sm_w = smem + L::off_w;
     uint8_t *sm_x = smem + L::off_x;
-    float *sm_sa = reinterpret_cast<float *>(smem + L::off_sa);
-    float *sm_sb = reinterpret_cast<float *>(smem + L::off_sb);
+    uint8_t *sm_sa = smem + L::off_sa;
+    uint8_t *sm_sb = smem + L::off_sb;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
@@ -645,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t kb0 = (int32_t)((int64_t)split * p.KB / p.S);
     const int32_t kb1 = (int32_t)((int64_t)(split + 1) * p.KB / p.S);
     const int32_t ngroups = kb1 - kb0;
+    const int32_t nbatch = (ngroups + GB - 1) / GB;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -653,13 +663,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < SC; ++i) {
             mbar_init(&sc_full[i], QX ? 2 : 1);        // QX: one arrival per quantizer warp
-            mbar_init(&sc_empty[i], kEpiWarps);
+            mbar_init(&sc_empty[i], kEpiWarps * 32);   // every promotion thread
         }
         if (QX)
             for (int i = 0; i < STAGES; ++i) mbar_init(&qfull[i], 2);
         for (int i = 0; i < L::nbuf; ++i) {
             mbar_init(&tm_full[i], 1);
-            mbar_init(&tm_empty[i], kEpiWarps);
+            mbar_init(&tm_empty[i], kEpiWarps * 32);
         }
         mbar_init(drain, 1);
         flags[0] = 0;
@@ -676,26 +686,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the control warpgroup gives back here (128*40 + 256*232 <= 384*168)
     if (warp < kEpiWarp0) regs_decrease<kCtrlRegs>();
 
+    // Waits on a stage, scale slot or TMEM buffer that has not been used yet
+    // are skipped: its first phase counts as released.
     if (warp == kProducerWarp) {
         if (elect_one()) {
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmX);
-            for (int32_t g = 0; g < ngroups; ++g) {
-                const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+            for (int32_t b = 0; b < nbatch; ++b) {
+                const uint32_t s = b % STAGES, ph = (b / STAGES) & 1;
+                if (b >= STAGES && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
                     record_timeout(p.status, kSiteProducerEmpty);
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(L::w_bytes + nt_run * BK * (QX ? 2 : 1)));
-                tma_load_2d(sm_w + s * L::w_bytes, &tmW, &full[s], (kb0 + g) * BK, (int32_t)(e * p.N) + tile * BM);
-                for (int32_t r = 0; r < nt_run; r += 16) {  // 16-row boxes: whole 128B-swizzle atoms
-                    if (QX)
-                        tma_load_2d(sm_xb + s * L::xb_bytes + r * BK * 2, &tmX, &full[s], (kb0 + g) * BK,
-                                    (int32_t)(e * p.cap) + r);
-                    else
-                        tma_load_2d(sm_x + s * L::x_bytes + r * BK, &tmX, &full[s], (kb0 + g) * BK,
-                                    (int32_t)(e * p.cap) + r);
+                const int32_t gn = min(GB, ngroups - b * GB);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(gn * (L::w_group + nt_run * BK * (QX ? 2 : 1))));
+                for (int32_t jj = 0; jj < gn; ++jj) {
+                    const int32_t kx = (kb0 + b * GB + jj) * BK;
+                    tma_load_2d(sm_w + s * L::w_bytes + jj * L::w_group, &tmW, &full[s], kx,
+                                (int32_t)(e * p.N) + tile * BM);
+                    for (int32_t r = 0; r < nt_run; r += 16) {   // 16-row boxes: whole 128B-swizzle atoms
+                        if (QX)
+                            tma_load_2d(sm_xb + s * L::xb_bytes + jj * L::xb_group + r * BK * 2, &tmX, &full[s], kx,
+                                        (int32_t)(e * p.cap) + r);
+                        else
+                            tma_load_2d(sm_x + s * L::x_bytes + jj * L::x_group + r * BK, &tmX, &full[s], kx,
+                                        (int32_t)(e * p.cap) + r);
+                    }
                 }
             }
         }
@@ -708,37 +725,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wq = (int)warp - kScaleWarp;
         const int c16 = (int)(lane & 15);
         bool ok = true;
-        for (int32_t g = 0; g < ngroups; ++g) {
-            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
-            const uint32_t j = g % SC, phj = (g / SC) & 1;
+        for (int32_t b = 0; b < nbatch; ++b) {
+            const uint32_t s = b % STAGES, ph = (b / STAGES) & 1;
+            const uint32_t j = b % SC, phj = (b / SC) & 1;
             if (!mbar_wait(&full[s], ph, abort_flag)) {
                 record_timeout(p.status, kSiteQuantFull);
                 ok = false;
                 break;
             }
-            if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+            if (b >= SC && !mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
                 record_timeout(p.status, kSiteProducerScale);
                 ok = false;
                 break;
             }
-            const uint8_t *xb = sm_xb + s * L::xb_bytes;
-            uint8_t *xq = sm_x + s * L::x_bytes;
-            for (int32_t r0 = 0; r0 < nt_run; r0 += 4) {
-                const int r = r0 + 2 * wq + (int)(lane >> 4);
-                float f[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xb + r * (BK * 2) + c16 * 16), f);
-                float a = amax8(f);
+            const int32_t gn = min(GB, ngroups - b * GB);
+            float *sav = reinterpret_cast<float *>(sm_sa + j * L::sa_slot);
+            float *sbv = reinterpret_cast<float *>(sm_sb + j * L::sb_slot);
+            for (int32_t jj = 0; jj < gn; ++jj) {
+                const uint8_t *xb = sm_xb + s * L::xb_bytes + jj * L::xb_group;
+                uint8_t *xq = sm_x + s * L::x_bytes + jj * L::x_group;
+                for (int32_t r0 = 0; r0 < nt_run; r0 += 4) {
+                    const int r = r0 + 2 * wq + (int)(lane >> 4);
+                    float f[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xb + r * (BK * 2) + c16 * 16), f);
+                    float a = amax8(f);
 #pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-                const float sc = __fdiv_rn(a, kE4M3Max);
-                const uint2 c = encode8(f, make_divisor(sc));
-                uint8_t *row = xq + (r >> 3) * 1024 + (r & 7) * 128;
-                *reinterpret_cast<uint2 *>(row + (((c16 >> 1) ^ (r & 7)) * 16) + (c16 & 1) * 8) = c;
-                if (c16 == 0) sm_sa[j * L::sa_slot + r] = sc;
+                    for (int o = 8; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                    const float sc = __fdiv_rn(a, kE4M3Max);
+                    const uint2 c = encode8(f, make_divisor(sc));
+                    uint8_t *row = xq + (r >> 3) * 1024 + (r & 7) * 128;
+                    *reinterpret_cast<uint2 *>(row + (((c16 >> 1) ^ (r & 7)) * 16) + (c16 & 1) * 8) = c;
+                    if (c16 == 0) sav[jj * NT + r] = sc;
+                }
+                if (wq == 0 && lane == 0)
+                    sbv[jj * 4 + (tile & 3)] = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + b * GB + jj) * p.ldsb + tile);
             }
-            if (wq == 0 && lane == 0)
-                sm_sb[j * 32 + (tile & 3)] = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + g) * p.ldsb + tile);
-            fence_proxy_async_smem();     // E4M3 tile -> the MMA; BF16 stage -> its next TMA refill
+            fence_proxy_async_smem();     // E4M3 tiles -> the MMA; BF16 stage -> its next TMA refill
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&qfull[s]);
@@ -747,45 +769,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) *abort_flag = 1;
     } else if (!QX && warp == kScaleWarp) {
+        // the scales of one batch: a (NT x GB) box of sa and a (4 x GB) box of
+        // the weight tile's block scales; boxes past the tensor read zeros
         if (elect_one()) {
             tma_prefetch_desc(&tmSA);
             tma_prefetch_desc(&tmSB);
-            for (int32_t g = 0; g < ngroups; ++g) {
-                const uint32_t j = g % SC, phj = (g / SC) & 1;
-                if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+            for (int32_t b = 0; b < nbatch; ++b) {
+                const uint32_t j = b % SC, phj = (b / SC) & 1;
+                if (b >= SC && !mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
                     record_timeout(p.status, kSiteProducerScale);
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(NT * 4 + 16));
-                tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + g);
-                tma_load_2d(sm_sb + j * 32, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + g);
+                mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(GB * NT * 4 + GB * 16));
+                tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + b * GB);
+                tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + b * GB);
             }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         const uint32_t idesc = idesc_e4m3_f32(BM, (uint32_t)nt_run);
         bool ok = true;
-        for (int32_t g = 0; g < ngroups; ++g) {
-            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
-            const uint32_t buf = g % L::nbuf, phb = (g / L::nbuf) & 1;
-            if (!mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
-                record_timeout(p.status, kSiteMmaTmemEmpty);
-                ok = false;
-                break;
-            }
+        for (int32_t b = 0; b < nbatch; ++b) {
+            const uint32_t s = b % STAGES, ph = (b / STAGES) & 1;
+            const uint32_t buf = b % L::nbuf, phb = (b / L::nbuf) & 1;
             if (!mbar_wait(QX ? &qfull[s] : &full[s], ph, abort_flag)) {
                 record_timeout(p.status, kSiteMmaFull);
                 ok = false;
                 break;
             }
+            if (b >= L::nbuf && !mbar_wait(&tm_empty[buf], phb ^ 1, abort_flag)) {
+                record_timeout(p.status, kSiteMmaTmemEmpty);
+                ok = false;
+                break;
+            }
             tc_fence_after_sync();
             if (elect_one()) {
-                const uint64_t dw = smem_desc_kmajor_sw128(sm_w + s * L::w_bytes);
-                const uint64_t dx = smem_desc_kmajor_sw128(sm_x + s * L::x_bytes);
+                const int32_t gn = min(GB, ngroups - b * GB);
+                for (int32_t jj = 0; jj < gn; ++jj) {
+                    const uint64_t dw = smem_desc_kmajor_sw128(sm_w + s * L::w_bytes + jj * L::w_group);
+                    const uint64_t dx = smem_desc_kmajor_sw128(sm_x + s * L::x_bytes + jj * L::x_group);
 #pragma unroll
-                for (int k = 0; k < BK / 32; ++k)
-                    mma_e4m3(tmem_base + buf * NT, dw + 2 * k, dx + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_e4m3(tmem_base + buf * L::bufcols + jj * NT, dw + 2 * k, dx + 2 * k, idesc,
+                                 k > 0 ? 1u : 0u);
+                }
                 mma_commit(&empty[s]);
                 mma_commit(&tm_full[buf]);
             }
@@ -806,42 +834,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < COLS / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
-        for (int32_t g = 0; g < ngroups; ++g) {
-            const uint32_t j = g % SC, phj = (g / SC) & 1;
+        for (int32_t b = 0; b < nbatch; ++b) {
+            const uint32_t j = b % SC, phj = (b / SC) & 1;
             if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
                 record_timeout(p.status, kSiteEpiScale);
                 ok = false;
                 break;
             }
-            const float sbw = sm_sb[j * 32 + (tile & 3)];
-            const float2 sbw2 = make_float2(sbw, sbw);
-            const float *sav = sm_sa + j * L::sa_slot + col0;
-            const uint32_t buf = g % L::nbuf, phb = (g / L::nbuf) & 1;
+            const uint32_t buf = b % L::nbuf, phb = (b / L::nbuf) & 1;
             if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
                 record_timeout(p.status, kSiteEpiTmemFull);
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
+            const int32_t gn = min(GB, ngroups - b * GB);
+            const float *sav = reinterpret_cast<const float *>(sm_sa + j * L::sa_slot);
+            const float *sbv = reinterpret_cast<const float *>(sm_sb + j * L::sb_slot);
 #pragma unroll
-            for (int c = 0; c < COLS; c += CH) {
-                if ((int32_t)(col0 + c) >= nt_run) break;      // no token columns left (warp-uniform)
-                uint32_t r[CH];
-                tmem_ld_sync<CH>(tmem_base + lane_addr + buf * NT + col0 + c, r);
+            for (int jj = 0; jj < GB; ++jj) {
+                if (jj >= gn) break;                            // warp-uniform
+                const float sbw = sbv[jj * 4 + (tile & 3)];
+                const float2 sbw2 = make_float2(sbw, sbw);
 #pragma unroll
-                for (int i = 0; i < CH / 2; ++i) {
-                    const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    const float2 sa2 = *reinterpret_cast<const float2 *>(sav + c + 2 * i);
-                    acc[c / 2 + i] = __ffma2_rn(pv, __fmul2_rn(sbw2, sa2), acc[c / 2 + i]);
+                for (int c = 0; c < COLS; c += CH) {
+                    if ((int32_t)(col0 + c) >= nt_run) break;  // no token columns left (warp-uniform)
+                    uint32_t r[CH];
+                    tmem_ld_sync<CH>(tmem_base + lane_addr + buf * L::bufcols + jj * NT + col0 + c, r);
+#pragma unroll
+                    for (int i = 0; i < CH / 2; ++i) {
+                        const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                        const float2 sa2 = *reinterpret_cast<const float2 *>(sav + jj * NT + col0 + c + 2 * i);
+                        acc[c / 2 + i] = __ffma2_rn(pv, __fmul2_rn(sbw2, sa2), acc[c / 2 + i]);
+                    }
                 }
             }
             fence_proxy_async_smem();         // scale slot j is refilled by TMA once released
             tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&tm_empty[buf]);
-                mbar_arrive(&sc_empty[j]);
-            }
+            mbar_arrive(&tm_empty[buf]);
+            mbar_arrive(&sc_empty[j]);
         }
         if (!ok) *abort_flag = 1;
         const int64_t n = (int64_t)tile * BM + wrow;
@@ -1275,10 +1306,10 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
                      : launch_variant<BN, STAGES, 8, 3, false, false>(a, p, grid, stream);
 }
 
-template <int NT, int STAGES, bool OUT_F32, bool QX = false>
+template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX = false>
 cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
-    using L = SmallLayout<NT, STAGES, 8, QX>;
+    using L = SmallLayout<NT, STAGES, SC, GB, QX>;
     SmallParams p{};
     p.M = a.M;
     p.N = a.N;
@@ -1308,11 +1339,11 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
         if (!make_tensor_map_2d(&tmX, 2, false, a.xbf16, a.K, (uint64_t)E * p.cap, a.ldx * 2, BK, 16, false))
             return cudaErrorInvalidValue;
     } else if (!make_tensor_map_2d(&tmX, 1, false, a.A, a.K, (uint64_t)E * p.cap, a.K, BK, 16, true) ||
-               !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, 1, false) ||
-               !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, 1, false)) {
+               !make_tensor_map_2d(&tmSA, 4, true, a.sa, a.ldsa, p.KB, a.ldsa * 4, NT, GB, false) ||
+               !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, GB, false)) {
         return cudaErrorInvalidValue;
     }
-    auto kern = gemm_smallm_kernel<NT, STAGES, 8, OUT_F32, QX>;
+    auto kern = gemm_smallm_kernel<NT, STAGES, SC, GB, OUT_F32, QX>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
     kern<<<E * p.n_tiles * p.S, kThreads, L::dyn_bytes, stream>>>(tmW, tmX, tmSA, tmSB, p);
@@ -1323,14 +1354,14 @@ template <bool OUT_F32>
 cudaError_t launch_small_nt(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
     switch (small_nt(a.counts != nullptr ? a.cap : a.M)) {
-    // as many weight stages as fit next to the token tiles (up to ~220 KB):
-    // a decode CTA streams only 8..14 K groups, so nearly all of them are in
-    // flight from the start instead of waiting for refills
-    case 16: return launch_small<16, 12, OUT_F32>(a, stream, num_sms);
-    case 32: return launch_small<32, 11, OUT_F32>(a, stream, num_sms);
-    case 64: return launch_small<64, 9, OUT_F32>(a, stream, num_sms);
-    case 128: return launch_small<128, 6, OUT_F32>(a, stream, num_sms);
-    default: return launch_small<256, 4, OUT_F32>(a, stream, num_sms);
+    // <tokens, stages, scale slots, K groups per batch>: batches of 4 K groups
+    // (2 and 1 where four partials would not fit in tensor memory), stages
+    // up to ~220 KB of shared memory
+    case 16: return launch_small<16, 3, 4, 4, OUT_F32>(a, stream, num_sms);
+    case 32: return launch_small<32, 2, 4, 4, OUT_F32>(a, stream, num_sms);
+    case 64: return launch_small<64, 2, 4, 4, OUT_F32>(a, stream, num_sms);
+    case 128: return launch_small<128, 3, 4, 2, OUT_F32>(a, stream, num_sms);
+    default: return launch_small<256, 4, 8, 1, OUT_F32>(a, stream, num_sms);
     }
 }
 
@@ -1426,10 +1457,14 @@ template <bool OUT_F32>
 cudaError_t launch_small_qx(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
     // stages so that the BF16 token staging fits next to the E4M3 tiles
+    // (the BF16 staging tile of 128 and 256 tokens takes 32 and 64 KB per K
+    // group: one group per stage, three stages and one)
     switch (small_nt(a.M)) {
-    case 16: return launch_small<16, 8, OUT_F32, true>(a, stream, num_sms);
-    case 32: return launch_small<32, 6, OUT_F32, true>(a, stream, num_sms);
-    default: return launch_small<64, 5, OUT_F32, true>(a, stream, num_sms);
+    case 16: return launch_small<16, 2, 4, 4, OUT_F32, true>(a, stream, num_sms);
+    case 32: return launch_small<32, 3, 4, 2, OUT_F32, true>(a, stream, num_sms);
+    case 64: return launch_small<64, 2, 4, 2, OUT_F32, true>(a, stream, num_sms);
+    case 128: return launch_small<128, 3, 4, 1, OUT_F32, true>(a, stream, num_sms);
+    default: return launch_small<256, 1, 4, 1, OUT_F32, true>(a, stream, num_sms);
     }
 }
 }  // namespace

@@ -42,7 +42,7 @@ struct GemmArgs {
     const int32_t *counts = nullptr;
     int64_t cap = 0;
     // token operand as BF16 [M][ldx], quantized 1x128 inside the GEMM
-    // (small M only); A and sa are unused then
+    // (M <= 256); A and sa are unused then
     const void *xbf16 = nullptr;
     int64_t ldx = 0;
 };
@@ -96,7 +96,7 @@ cudaError_t launch_pair(const GemmArgs &a, cudaStream_t stream);
 size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);
 size_t masked_workspace_zeroed_bytes(int32_t num_experts, int64_t N);
 cudaError_t launch_masked(const GemmArgs &a, cudaStream_t stream, int num_sms);
-// Token operand given as BF16 and quantized in the GEMM's producer (M <= 64).
+// Token operand given as BF16 and quantized in the GEMM's producer (M <= 256).
 cudaError_t launch_bf16a(const GemmArgs &a, cudaStream_t stream, int num_sms);
 cudaError_t launch_mma_probe(const uint8_t *A, const uint8_t *B, float *D, int N, int K, void *workspace,
                              cudaStream_t stream);

@@ -242,7 +242,7 @@ fgf8_status fgf8_noalloc_read_status(void *stream, int32_t *site);
  * of fp8_quant_act_1x128 (same rule, same arithmetic), so the result equals
  * fp8_quant_act_1x128 followed by fp8_gemm_blockscaled bit for bit.
  *
- *   x  : BF16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.  1 <= M <= 64.
+ *   x  : BF16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.  1 <= M <= 256.
  *   B  : E4M3 [N][K] with 128x128 block scales sb [K/128][ldsb] as in
  *        fp8_gemm_blockscaled (BLOCK128 kind).  N % 16 == 0, K % 128 == 0.
  *   C  : [M][ldc] BF16 or FP32, as in fp8_gemm_blockscaled.

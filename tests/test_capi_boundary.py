@@ -165,7 +165,7 @@ def test_bf16a_rejects(L):
 
     assert call(M=0, x=None) == 0                # empty output: nothing touched
     assert call(x=None) == 1
-    assert call(M=65) == 3                       # at most 64 tokens
+    assert call(M=257) == 3                      # at most 256 tokens
     assert call(K=200, ldx=200) == 3
     assert call(N=250, ldc=256) == 3
     assert call(ldx=256) == 1                    # ldx < K

@@ -540,11 +540,12 @@ def test_full_size_moe_decode_sampled():
                 assert_within_bound(Cg[e, r:r + 1], Cr[e, r:r + 1], S[e, r:r + 1], f"moe decode expert {e} row {r}")
 
 
-# --- token operand given as BF16, quantized inside the GEMM (decode M <= 64) ---
+# --- token operand given as BF16, quantized inside the GEMM (decode M <= 256) ---
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 7168), (5, 144, 2048), (33, 512, 1024), (64, 7168, 2048),
-                                   (64, 256, 128), (1, 16, 256)])
+                                   (64, 256, 128), (1, 16, 256), (128, 4096, 7168), (100, 512, 1024),
+                                   (256, 7168, 2048), (200, 1024, 640)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
 def test_bf16a_equals_quantize_then_gemm(M, N, K, out):
     # same rule and arithmetic as the quantization kernel: the fused GEMM must
@@ -581,7 +582,7 @@ def test_bf16a_row_stride_and_rejects_large_m():
     torch.cuda.synchronize()
     assert torch.equal(fused.view(torch.int16), twostep.view(torch.int16))
     with pytest.raises(fg.FGF8Error, match="UNSUPPORTED_SHAPE"):
-        fg.fp8_gemm_bf16a_blockscaled(dev_bf16(wl.bf16_normal(rng, (65, 512))), qb, sb)
+        fg.fp8_gemm_bf16a_blockscaled(dev_bf16(wl.bf16_normal(rng, (257, 512))), qb, sb)
 
 
 # One workspace serves every GEMM kernel in turn: the split kernels' arrival
