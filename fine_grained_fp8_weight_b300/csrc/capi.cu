@@ -293,7 +293,8 @@ fgf8_status fp8_masked_grouped_gemm_blockscaled(const uint8_t *A, const float *s
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(4) << 20;        // 4 MiB per device
+constexpr size_t kStaticScratchBytes = size_t(4) << 10;        // 4 KiB per device: status header and counters
+static_assert(kStaticScratchBytes >= fgf8::kWsPartialsOffset, "the cleared header and counters fit");
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mutex;
@@ -334,7 +335,7 @@ fgf8_status fp8_gemm_blockscaled_noalloc(const uint8_t *A, const float *sa, int6
     fgf8::GemmArgs a{A, sa, ldsa, B, sb, ldsb, (int)bkind, C, ldc, cdt == FGF8_OUT_FP32 ? 1 : 0, M, N, K,
                      nullptr, 1, ws, kStaticScratchBytes};
     // the scratch the schedule for this shape really uses (on this device,
-    // with 4 MiB of scratch) must fit
+    // with this scratch) must fit
     if (fgf8::gemm_required_bytes(a, num_sms) > kStaticScratchBytes) return FGF8_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // the previous call's status word (and split-K counters) must not leak into this one
@@ -420,6 +421,13 @@ fgf8_status fgf8_testing_set_pair(int32_t mode)
 {
     if (mode != 0 && mode != 1) return FGF8_ERR_INVALID_ARG;
     fgf8::set_pair_mode(mode);
+    return FGF8_OK;
+}
+
+fgf8_status fgf8_testing_set_small_splits(int32_t splits)
+{
+    if (splits < 0 || splits > 8) return FGF8_ERR_INVALID_ARG;
+    fgf8::set_small_splits(splits);
     return FGF8_OK;
 }
 

@@ -30,8 +30,9 @@
 //   the FP32 partials in K order and writes the tile.  No CTA waits for
 //   another.
 // gemm_smallm_kernel (decode, M <= 256 tokens): the weight tile takes the
-// MMA's M side and the tokens its N side, K is split over CTAs with an
-// in-order reduction; the same kernel serves the masked grouped layout
+// MMA's M side and the tokens its N side, K is split over the CTAs of a
+// thread-block cluster, which add their partials in split order through
+// distributed shared memory; the same kernel serves the masked grouped layout
 // (per-expert token slots with device-side counts) and, for M <= 256, the
 // variant that quantizes BF16 tokens inside the kernel.
 #include <cuda.h>
@@ -544,21 +545,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // read 128 x K bytes of weights per 2*128*NT*K FLOP, far below the tensor
 // cores' ridge ("kailasan.com recruit post 147436", decode passage: the batch
 // per expert is small and memory access is the bottleneck), so the K groups
-// are split across CTAs until every SM streams weights.  Each split's FP32
-// partial goes to the workspace; the last CTA of a weight tile to take an
-// atomic ticket adds the partials in split order (deterministic), writes the
-// output and resets the ticket.  No CTA waits for another.
+// are split across CTAs until the SMs stream weights.  The S splits of one
+// weight tile form a thread-block cluster: after its last K group each CTA
+// leaves its FP32 partial in its own (by then idle) stage memory, the cluster
+// synchronises once, and CTA r adds the r-th slice of all S partials in split
+// order (deterministic) straight from the peers' shared memory and writes
+// that slice of the output; a second cluster barrier keeps every CTA resident
+// until its partial has been read.  Nothing goes through global memory but
+// the output.
 // Promotion: acc[token] += P[w_row][token] * (sb[w block][kb] * sa[kb][token]).
 // ------------------------------------------------------------------------
-constexpr int kMaxSplits = 8;   // split-K factor of the small-M kernel, at most
+constexpr int kMaxSplits = 8;   // split-K factor (= cluster size) of the small-M kernel, at most
 
 struct SmallParams {
     int64_t M, N, K;
-    int32_t KB, S, n_tiles;
+    int32_t KB, S, n_tiles;   // S: CTAs per cluster (blockIdx.x mod S = split = cluster rank)
     void *C;
     int64_t ldc;
-    float *partials;          // [experts][n_tiles][S][NT][128]
-    uint32_t *tickets;        // [experts][n_tiles], zero between calls
     DeviceStatus *status;
     // masked grouped layout (decode MoE): expert e owns token rows
     // e*cap .. e*cap+cap-1 of A and C (and those columns of sa) and weight
@@ -587,13 +590,17 @@ struct SmallLayout {
     static constexpr size_t off_xb = align_up(off_x + STAGES * x_bytes, 1024);
     static constexpr size_t sa_slot = align_up((size_t)GB * NT * 4, 128);   // [GB][NT] floats (a TMA box)
     static constexpr size_t sb_slot = align_up((size_t)GB * 16, 128);       // [GB][4] floats (a TMA box)
-    static constexpr size_t off_sa = align_up(off_xb + STAGES * xb_bytes, 1024);
+    // the split's FP32 partial [NT][128] reuses the stage memory after the
+    // last K group (extended where the stages are smaller)
+    static constexpr size_t part_bytes = (size_t)NT * BM * 4;
+    static constexpr size_t stage_end = align_up(off_xb + STAGES * xb_bytes, 1024);
+    static constexpr size_t off_sa = stage_end > part_bytes ? stage_end : part_bytes;
     static constexpr size_t off_sb = off_sa + (size_t)SC * sa_slot;
     static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * sb_slot, 16);
     static constexpr int bufcols = GB * NT;                    // TMEM columns of one batch's partials
     // as many TMEM buffers as fit (up to 8): the MMA runs that many batches ahead
     static constexpr int nbuf = (512 / bufcols) < 8 ? (512 / bufcols) : 8;
-    static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1 + (QX ? STAGES : 0);
+    static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1 + (QX ? STAGES : SC);
     static constexpr size_t off_misc = off_bar + (size_t)num_bars * 8;
     static constexpr size_t total = off_misc + 16;
     static constexpr size_t dyn_bytes = total + 1024;
@@ -629,9 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tm_empty = tm_full + L::nbuf;
     uint64_t *drain = tm_full + 2 * L::nbuf;
     uint64_t *qfull = drain + 1;                 // QX: stage s quantized (after full[s])
+    uint64_t *pr_full = drain + 1;               // not QX: scale slot j holds the products sb * sa
     uint8_t *sm_xb = smem + L::off_xb;
     uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + L::off_misc + 4);   // [0] abort, [1] last
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + L::off_misc + 4);   // [0] abort, [1] partial ok
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
@@ -640,7 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t rem = blockIdx.x - e * per_expert;
     const int32_t tile = rem / p.S;              // 128 weight rows
     const int32_t split = rem - tile * p.S;
-    const int32_t et = e * p.n_tiles + tile;     // (expert, weight tile)
     int64_t m_real = p.M;                        // token columns that are written
     if (p.counts != nullptr) {
         int32_t c = __ldg(p.counts + e);
@@ -667,6 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (QX)
             for (int i = 0; i < STAGES; ++i) mbar_init(&qfull[i], 2);
+        else
+            for (int i = 0; i < SC; ++i) mbar_init(&pr_full[i], 1);
         for (int i = 0; i < L::nbuf; ++i) {
             mbar_init(&tm_full[i], 1);
             mbar_init(&tm_empty[i], kEpiWarps * 32);
@@ -675,6 +684,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         flags[0] = 0;
         flags[1] = 0;
         fence_barrier_init();
+    }
+    // one batch of weight and token tiles into stage b % STAGES
+    auto issue_batch = [&](int32_t b) {
+        const uint32_t s = b % STAGES;
+        const int32_t gn = min(GB, ngroups - b * GB);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(gn * (L::w_group + nt_run * BK * (QX ? 2 : 1))));
+        for (int32_t jj = 0; jj < gn; ++jj) {
+            const int32_t kx = (kb0 + b * GB + jj) * BK;
+            tma_load_2d(sm_w + s * L::w_bytes + jj * L::w_group, &tmW, &full[s], kx, (int32_t)(e * p.N) + tile * BM);
+            for (int32_t r = 0; r < nt_run; r += 16) {   // 16-row boxes: whole 128B-swizzle atoms
+                if (QX)
+                    tma_load_2d(sm_xb + s * L::xb_bytes + jj * L::xb_group + r * BK * 2, &tmX, &full[s], kx,
+                                (int32_t)(e * p.cap) + r);
+                else
+                    tma_load_2d(sm_x + s * L::x_bytes + jj * L::x_group + r * BK, &tmX, &full[s], kx,
+                                (int32_t)(e * p.cap) + r);
+            }
+        }
+    };
+    // the scales of batch b: a (NT x GB) box of sa and a (4 x GB) box of the
+    // weight tile's block scales; boxes past the tensor read zeros
+    auto issue_scales = [&](int32_t b) {
+        const uint32_t j = b % SC;
+        mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(GB * NT * 4 + GB * 16));
+        tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + b * GB);
+        tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + b * GB);
+    };
+    // The first batch goes out before the block-wide barrier (the TMEM
+    // allocation runs meanwhile): its stage and scale slot are unused, and
+    // this thread initialised the barriers they complete on.  (Issuing every
+    // free stage here would hold the other warps at the barrier while the
+    // TMA unit accepts the copies.)
+    const int32_t pre_w = 1;
+    const int32_t pre_s = QX ? 0 : 1;
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+        if (!QX) {
+            tma_prefetch_desc(&tmSA);
+            tma_prefetch_desc(&tmSB);
+        }
+        for (int32_t b = 0; b < pre_w; ++b) issue_batch(b);
+        for (int32_t b = 0; b < pre_s; ++b) issue_scales(b);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_base_slot, L::tmem_cols);
     tc_fence_before_sync();
@@ -690,30 +742,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are skipped: its first phase counts as released.
     if (warp == kProducerWarp) {
         if (elect_one()) {
-            tma_prefetch_desc(&tmW);
-            tma_prefetch_desc(&tmX);
-            for (int32_t b = 0; b < nbatch; ++b) {
+            for (int32_t b = pre_w; b < nbatch; ++b) {
                 const uint32_t s = b % STAGES, ph = (b / STAGES) & 1;
-                if (b >= STAGES && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
                     record_timeout(p.status, kSiteProducerEmpty);
                     *abort_flag = 1;
                     break;
                 }
-                const int32_t gn = min(GB, ngroups - b * GB);
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(gn * (L::w_group + nt_run * BK * (QX ? 2 : 1))));
-                for (int32_t jj = 0; jj < gn; ++jj) {
-                    const int32_t kx = (kb0 + b * GB + jj) * BK;
-                    tma_load_2d(sm_w + s * L::w_bytes + jj * L::w_group, &tmW, &full[s], kx,
-                                (int32_t)(e * p.N) + tile * BM);
-                    for (int32_t r = 0; r < nt_run; r += 16) {   // 16-row boxes: whole 128B-swizzle atoms
-                        if (QX)
-                            tma_load_2d(sm_xb + s * L::xb_bytes + jj * L::xb_group + r * BK * 2, &tmX, &full[s], kx,
-                                        (int32_t)(e * p.cap) + r);
-                        else
-                            tma_load_2d(sm_x + s * L::x_bytes + jj * L::x_group + r * BK, &tmX, &full[s], kx,
-                                        (int32_t)(e * p.cap) + r);
-                    }
-                }
+                issue_batch(b);
             }
         }
         __syncwarp();
@@ -740,10 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int32_t gn = min(GB, ngroups - b * GB);
             float *sav = reinterpret_cast<float *>(sm_sa + j * L::sa_slot);
-            float *sbv = reinterpret_cast<float *>(sm_sb + j * L::sb_slot);
             for (int32_t jj = 0; jj < gn; ++jj) {
                 const uint8_t *xb = sm_xb + s * L::xb_bytes + jj * L::xb_group;
                 uint8_t *xq = sm_x + s * L::x_bytes + jj * L::x_group;
+                const float sbw = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + b * GB + jj) * p.ldsb + tile);
                 for (int32_t r0 = 0; r0 < nt_run; r0 += 4) {
                     const int r = r0 + 2 * wq + (int)(lane >> 4);
                     float f[8];
@@ -755,10 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint2 c = encode8(f, make_divisor(sc));
                     uint8_t *row = xq + (r >> 3) * 1024 + (r & 7) * 128;
                     *reinterpret_cast<uint2 *>(row + (((c16 >> 1) ^ (r & 7)) * 16) + (c16 & 1) * 8) = c;
-                    if (c16 == 0) sav[jj * NT + r] = sc;
+                    if (c16 == 0) sav[jj * NT + r] = sbw * sc;   // the promotion's scale of this token
                 }
-                if (wq == 0 && lane == 0)
-                    sbv[jj * 4 + (tile & 3)] = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + b * GB + jj) * p.ldsb + tile);
             }
             fence_proxy_async_smem();     // E4M3 tiles -> the MMA; BF16 stage -> its next TMA refill
             __syncwarp();
@@ -768,22 +802,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) *abort_flag = 1;
+    } else if (!QX && warp == kScaleWarp + 1) {
+        // The promotion's per-token scale of each K group, sb(weight block) *
+        // sa(token), formed once per CTA in place in the scale slot (instead of
+        // once per weight row by every promotion thread).
+        for (int32_t b = 0; b < nbatch; ++b) {
+            const uint32_t j = b % SC, phj = (b / SC) & 1;
+            if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
+                record_timeout(p.status, kSiteEpiScale);
+                *abort_flag = 1;
+                break;
+            }
+            const int32_t gn = min(GB, ngroups - b * GB);
+            float *sav = reinterpret_cast<float *>(sm_sa + j * L::sa_slot);
+            const float *sbv = reinterpret_cast<const float *>(sm_sb + j * L::sb_slot);
+            for (int32_t jj = 0; jj < gn; ++jj) {
+                const float sbw = sbv[jj * 4 + (tile & 3)];
+                for (int32_t t = (int32_t)lane; t < nt_run; t += 32) sav[jj * NT + t] = sbw * sav[jj * NT + t];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pr_full[j]);
+        }
     } else if (!QX && warp == kScaleWarp) {
-        // the scales of one batch: a (NT x GB) box of sa and a (4 x GB) box of
-        // the weight tile's block scales; boxes past the tensor read zeros
         if (elect_one()) {
-            tma_prefetch_desc(&tmSA);
-            tma_prefetch_desc(&tmSB);
-            for (int32_t b = 0; b < nbatch; ++b) {
+            for (int32_t b = pre_s; b < nbatch; ++b) {
                 const uint32_t j = b % SC, phj = (b / SC) & 1;
-                if (b >= SC && !mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
+                if (!mbar_wait(&sc_empty[j], phj ^ 1, abort_flag)) {
                     record_timeout(p.status, kSiteProducerScale);
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(GB * NT * 4 + GB * 16));
-                tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + b * GB);
-                tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + b * GB);
+                issue_scales(b);
             }
         }
         __syncwarp();
@@ -836,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int32_t b = 0; b < nbatch; ++b) {
             const uint32_t j = b % SC, phj = (b / SC) & 1;
-            if (!mbar_wait(&sc_full[j], phj, abort_flag)) {
+            if (!mbar_wait(QX ? &sc_full[j] : &pr_full[j], phj, abort_flag)) {
                 record_timeout(p.status, kSiteEpiScale);
                 ok = false;
                 break;
@@ -849,23 +898,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const int32_t gn = min(GB, ngroups - b * GB);
-            const float *sav = reinterpret_cast<const float *>(sm_sa + j * L::sa_slot);
-            const float *sbv = reinterpret_cast<const float *>(sm_sb + j * L::sb_slot);
+            // per token: sb(weight block) * sa(token), the same for every weight row
+            const float *scl = reinterpret_cast<const float *>(sm_sa + j * L::sa_slot);
 #pragma unroll
             for (int jj = 0; jj < GB; ++jj) {
                 if (jj >= gn) break;                            // warp-uniform
-                const float sbw = sbv[jj * 4 + (tile & 3)];
-                const float2 sbw2 = make_float2(sbw, sbw);
 #pragma unroll
                 for (int c = 0; c < COLS; c += CH) {
                     if ((int32_t)(col0 + c) >= nt_run) break;  // no token columns left (warp-uniform)
                     uint32_t r[CH];
                     tmem_ld_sync<CH>(tmem_base + lane_addr + buf * L::bufcols + jj * NT + col0 + c, r);
 #pragma unroll
-                    for (int i = 0; i < CH / 2; ++i) {
-                        const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                        const float2 sa2 = *reinterpret_cast<const float2 *>(sav + jj * NT + col0 + c + 2 * i);
-                        acc[c / 2 + i] = __ffma2_rn(pv, __fmul2_rn(sbw2, sa2), acc[c / 2 + i]);
+                    for (int i = 0; i < CH / 4; ++i) {
+                        const float4 s4 = *reinterpret_cast<const float4 *>(scl + jj * NT + col0 + c + 4 * i);
+                        const float2 p0 = make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]));
+                        const float2 p1 = make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                        acc[c / 2 + 2 * i] = __ffma2_rn(p0, make_float2(s4.x, s4.y), acc[c / 2 + 2 * i]);
+                        acc[c / 2 + 2 * i + 1] = __ffma2_rn(p1, make_float2(s4.z, s4.w), acc[c / 2 + 2 * i + 1]);
                     }
                 }
             }
@@ -893,55 +942,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (p.S > 1) {
-            // this split's partial: [column][weight row], one 128-byte row per warp store
-            float *part = p.partials + ((int64_t)et * p.S + split) * NT * BM;
+            // this split's partial, [token column][weight row], into this CTA's
+            // stage memory: every TMA load into it has landed and every MMA
+            // reading it has completed (the last tm_full wait above)
+            float *part = reinterpret_cast<float *>(smem + L::off_w);
             if (ok) {
 #pragma unroll
                 for (int i = 0; i < COLS / 2; ++i) {
-                    part[(int64_t)(col0 + 2 * i) * BM + wrow] = acc[i].x;
-                    part[(int64_t)(col0 + 2 * i + 1) * BM + wrow] = acc[i].y;
+                    part[(col0 + 2 * i) * BM + wrow] = acc[i].x;
+                    part[(col0 + 2 * i + 1) * BM + wrow] = acc[i].y;
                 }
             }
-            __threadfence();
-            // all eight promotion warps have written; none gave up?
-            const bool all_ok = named_barrier_and(1, kEpiWarps * 32, ok && !*abort_flag);
-            if (all_ok && threadIdx.x == kEpiWarp0 * 32) {
-                const uint32_t ticket = atomicAdd(p.tickets + et, 1u);
-                const int last = ticket == (uint32_t)p.S - 1;
-                if (last) p.tickets[et] = 0u;                   // ready for the next call
-                flags[1] = last;
+            // all eight promotion warps done, none gave up?
+            const bool mine_ok = named_barrier_and(1, kEpiWarps * 32, ok && !*abort_flag);
+            if (threadIdx.x == kEpiWarp0 * 32) flags[1] = mine_ok ? 1 : 0;
+            // Split-K reduction across the cluster.  Every thread of every CTA
+            // in the cluster passes both cluster barriers (the other warps at
+            // the end of the kernel); the CTAs of one cluster share the
+            // expert, so an idle expert's CTAs have all returned above.
+            __syncwarp();
+            cluster_sync();                      // partials and ok flags visible cluster-wide
+            uint32_t peer[kMaxSplits];
+            int32_t peer_ok[kMaxSplits];
+#pragma unroll
+            for (int q = 0; q < kMaxSplits; ++q) {
+                if (q < p.S) {
+                    peer[q] = cluster_map(smem + L::off_w, (uint32_t)q);
+                    peer_ok[q] = ld_cluster_s32(cluster_map((const void *)&flags[1], (uint32_t)q));
+                }
             }
-            named_barrier_sync(1, kEpiWarps * 32);
-            if (all_ok && flags[1]) {
-                // last split of this weight tile: add the partials in split
-                // order, four outputs per float4, kRedUnroll of them in flight
-                __threadfence();
+            bool all_ok = true;
+#pragma unroll
+            for (int q = 0; q < kMaxSplits; ++q)
+                if (q < p.S) all_ok = all_ok && peer_ok[q] != 0;
+            if (all_ok) {
+                // slice `split` of the computed float4s (four outputs each),
+                // summed over the splits in order; kRedUnroll float4s of every
+                // split in flight per thread
                 constexpr int kRedUnroll = 4;
-                constexpr int E4s = NT * BM / 4;                // float4 per partial (its stride)
-                const int E4 = nt_run * BM / 4;                 // the computed token columns
-                const float4 *base = reinterpret_cast<const float4 *>(p.partials + (int64_t)et * p.S * NT * BM);
+                constexpr int kStride = kEpiWarps * 32;
+                const int E4 = nt_run * BM / 4;
+                const int lo = split * E4 / p.S, hi = (split + 1) * E4 / p.S;
                 const int t = (int)threadIdx.x - kEpiWarp0 * 32;   // 0 .. 255
-                for (int e0 = t; e0 < E4; e0 += kEpiWarps * 32 * kRedUnroll) {
+                for (int e0 = lo + t; e0 < hi; e0 += kStride * kRedUnroll) {
                     float4 v[kRedUnroll][kMaxSplits];
 #pragma unroll
                     for (int u = 0; u < kRedUnroll; ++u) {
-                        const int e4 = e0 + u * kEpiWarps * 32;
+                        const int e4 = e0 + u * kStride;
 #pragma unroll
-                        for (int sidx = 0; sidx < kMaxSplits; ++sidx)
-                            if (sidx < p.S && e4 < E4) v[u][sidx] = __ldcg(base + (int64_t)sidx * E4s + e4);
+                        for (int q = 0; q < kMaxSplits; ++q)
+                            if (q < p.S && e4 < hi) v[u][q] = ld_cluster_f4(peer[q] + (uint32_t)e4 * 16u);
                     }
 #pragma unroll
                     for (int u = 0; u < kRedUnroll; ++u) {
-                        const int e4 = e0 + u * kEpiWarps * 32;
-                        if (e4 >= E4) continue;
+                        const int e4 = e0 + u * kStride;
+                        if (e4 >= hi) break;
                         float4 sum = v[u][0];
 #pragma unroll
-                        for (int sidx = 1; sidx < kMaxSplits; ++sidx) {
-                            if (sidx < p.S) {
-                                sum.x += v[u][sidx].x;
-                                sum.y += v[u][sidx].y;
-                                sum.z += v[u][sidx].z;
-                                sum.w += v[u][sidx].w;
+                        for (int q = 1; q < kMaxSplits; ++q) {
+                            if (q < p.S) {
+                                sum.x += v[u][q].x;
+                                sum.y += v[u][q].y;
+                                sum.z += v[u][q].z;
+                                sum.w += v[u][q].w;
                             }
                         }
                         const int col = (e4 * 4) / BM, r = e4 * 4 - col * BM;
@@ -951,17 +1014,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (OUT_F32) {
                             *reinterpret_cast<float4 *>(static_cast<float *>(p.C) + row * p.ldc + n) = sum;
                         } else {
-                            const __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x, sum.y);
-                            const __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z, sum.w);
+                            const __nv_bfloat162 lo2 = __floats2bfloat162_rn(sum.x, sum.y);
+                            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(sum.z, sum.w);
                             uint2 o;
-                            memcpy(&o.x, &lo, 4);
-                            memcpy(&o.y, &hi, 4);
+                            memcpy(&o.x, &lo2, 4);
+                            memcpy(&o.y, &hi2, 4);
                             *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.C) + row * p.ldc + n) = o;
                         }
                     }
                 }
             }
+            __syncwarp();
+            cluster_sync();                      // no CTA leaves while a peer still reads its partial
         }
+    }
+    if (p.S > 1 && warp < kEpiWarp0) {
+        // the control warps' part in the two cluster barriers of the reduction
+        __syncwarp();
+        cluster_sync();
+        cluster_sync();
     }
 
     tc_fence_before_sync();
@@ -1148,9 +1219,12 @@ bool use_small_m(int64_t M, int64_t N, int32_t num_experts_or_dense, int num_sms
     return M <= 256 && (N + BM - 1) / BM <= (num_sms > 0 ? num_sms / 2 : 74);
 }
 
+int g_small_splits = 0;     // testing: forced split count of the dense small-M kernel (0: planner)
+
 int small_splits(int64_t N, int64_t K, int num_sms)
 {
     const int64_t tiles = (N + BM - 1) / BM, KB = K / BK;
+    if (g_small_splits > 0) return (int)(g_small_splits < KB ? g_small_splits : KB);
     int64_t S = (num_sms > 0 ? num_sms : 148) / tiles;
     if (S > kMaxSplits) S = kMaxSplits;
     if (S > KB) S = KB;
@@ -1209,24 +1283,16 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts
     return bytes;
 }
 
-size_t gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts)
+size_t gemm_workspace_min_bytes(int64_t, int64_t, int64_t, int32_t)
 {
-    size_t bytes = kWsHeaderBytes;
-    if (num_experts <= 1 && M <= 256) {
-        // small-M split-K: arrival tickets and FP32 partials, sized for the
-        // largest split count any device could choose
-        const int64_t tiles = (N + BM - 1) / BM;
-        const int64_t smax = K / BK < kMaxSplits ? K / BK : kMaxSplits;
-        bytes = kWsPartialsOffset + (size_t)tiles * smax * small_nt(M) * BM * 4;
-    }
-    return bytes;
+    // whole tiles, and the small-M split (reduced within its cluster), need
+    // the status header alone
+    return kWsHeaderBytes;
 }
 
-size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K)
+size_t masked_workspace_bytes(int32_t, int64_t, int64_t, int64_t)
 {
-    const int64_t tiles = (N + BM - 1) / BM;
-    const int S = masked_splits(num_experts, tiles, K / BK);
-    return S > 1 ? kWsPartialsOffset + (size_t)num_experts * tiles * S * small_nt(cap) * BM * 4 : kWsHeaderBytes;
+    return kWsHeaderBytes;
 }
 
 size_t masked_workspace_zeroed_bytes(int32_t, int64_t)
@@ -1318,17 +1384,13 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     p.n_tiles = (int32_t)((a.N + BM - 1) / BM);
     const int32_t E = a.counts != nullptr ? a.num_experts : 1;
     p.S = a.counts != nullptr ? masked_splits(E, p.n_tiles, p.KB) : small_splits(a.N, a.K, num_sms);
-    if ((int64_t)E * p.n_tiles > kMaxCounters) p.S = 1;    // no counters needed without a split
     p.C = a.C;
     p.ldc = a.ldc;
     p.counts = a.counts;
     p.cap = a.counts != nullptr ? a.cap : a.M;
     p.sb = a.sb;
     p.ldsb = a.ldsb;
-    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-    p.status = reinterpret_cast<DeviceStatus *>(ws);
-    p.tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
-    p.partials = reinterpret_cast<float *>(ws + kWsPartialsOffset);
+    p.status = reinterpret_cast<DeviceStatus *>(a.workspace);
     CUtensorMap tmW, tmX, tmSA, tmSB;
     memset(&tmSA, 0, sizeof(tmSA));
     memset(&tmSB, 0, sizeof(tmSB));
@@ -1346,8 +1408,20 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
     auto kern = gemm_smallm_kernel<NT, STAGES, SC, GB, OUT_F32, QX>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
-    kern<<<E * p.n_tiles * p.S, kThreads, L::dyn_bytes, stream>>>(tmW, tmX, tmSA, tmSB, p);
-    return cudaGetLastError();
+    // the S splits of a weight tile: one cluster of S consecutive CTAs
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(E * p.n_tiles * p.S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::dyn_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, tmSA, tmSB, p);
 }
 
 template <bool OUT_F32>
@@ -1396,11 +1470,17 @@ void set_pair_mode(int mode)
     g_pair_mode = mode;
 }
 
+void set_small_splits(int s)
+{
+    g_small_splits = s;
+}
+
 GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
 {
     GemmSchedule g{};
     if (a.m_indices == nullptr && a.bkind == 0 && use_small_m(a.M, a.N, 1, num_sms)) {
         g.small_m = 1;
+        g.tail_s = small_splits(a.N, a.K, num_sms);
         return g;
     }
     if (use_pair(a)) {
@@ -1423,13 +1503,6 @@ GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
 size_t gemm_required_bytes(const GemmArgs &a, int num_sms)
 {
     const GemmSchedule g = gemm_schedule(a, num_sms);
-    if (g.small_m) {
-        // small-M split-K: the arrival tickets and the FP32 partials of the
-        // split count this device uses (none without a split)
-        const int64_t tiles = (a.N + BM - 1) / BM;
-        const int S = tiles > kMaxCounters ? 1 : small_splits(a.N, a.K, num_sms);
-        return S > 1 ? kWsPartialsOffset + (size_t)tiles * S * small_nt(a.M) * BM * 4 : kWsHeaderBytes;
-    }
     if (g.tail_s > 1) return g.pair ? pair_tail_workspace_bytes() : tail_workspace_bytes(g.bn);
     return kWsHeaderBytes;
 }

@@ -73,6 +73,7 @@ GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms);
 // 1: dense block-scaled GEMMs of more than 128 rows run on CTA pairs; 0: the
 // planner's choice (single-SM tiles).  Process-wide, for tests.
 void set_pair_mode(int mode);
+void set_small_splits(int s);
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
 // Workspace bytes the schedule launch_gemm picks for `a` (with a.ws_bytes of
 // workspace) reads and writes: the status header, plus the split kernels'

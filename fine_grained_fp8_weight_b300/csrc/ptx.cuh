@@ -325,8 +325,8 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-// Every thread of both CTAs arrives, then waits for all of them.  Memory
-// operations before it are visible to the whole cluster after it.
+// Every thread of every CTA in the cluster arrives, then waits for all of
+// them.  Memory operations before it are visible to the whole cluster after it.
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -340,6 +340,25 @@ __device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank)
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
     return r;
+}
+
+// 16-byte load from the shared memory of a CTA of this cluster (address from
+// cluster_map).
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_cluster_s32(uint32_t addr)
+{
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // Arrive on an mbarrier given by its cluster address (possibly in the other

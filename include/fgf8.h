@@ -162,9 +162,12 @@ fgf8_status fp8_quant_w_128x128_t(const void *w, int64_t N, int64_t K, int64_t l
  *   C  : [M][ldc] BF16 (cdt = FGF8_OUT_BF16) or FP32 (FGF8_OUT_FP32); ldc >= N,
  *        ldc * element size % 16 == 0, 16-byte aligned.
  *   workspace : device scratch of at least fgf8_gemm_workspace_min_bytes(M, N,
- *        K, 1) bytes, 256-byte aligned, ZERO-FILLED before its first use.  It
- *        holds the device status word and, for small M, the split-K partial
- *        sums and arrival counters.  With fgf8_gemm_workspace_bytes(M, N, K, 1)
+ *        K, 1) bytes (256), 256-byte aligned, ZERO-FILLED before its first
+ *        use.  It holds the device status word.  (For small M the K groups of
+ *        each 128-row weight tile are split over the CTAs of one thread-block
+ *        cluster, which add their FP32 partials in split order through
+ *        distributed shared memory: no workspace.)  With
+ *        fgf8_gemm_workspace_bytes(M, N, K, 1)
  *        bytes it also holds the last-wave split: when the output tiles leave
  *        the last wave over the SMs partly empty, those tail tiles are cut
  *        along K into pieces that run on the idle SMs, and the last piece of
@@ -195,23 +198,20 @@ fgf8_status fp8_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa
  *
  * Same arguments, layouts, checks and result as fp8_gemm_blockscaled, minus
  * the workspace.  It allocates nothing (no cudaMalloc, no cudaFree, no
- * allocating library routine): its scratch is a 4 MiB array in device global
+ * allocating library routine): its scratch is a 4 KiB array in device global
  * memory that every device loading the library holds until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress) with the device current; make that first call
  *     before any stream capture on the device.
  *   - The scratch a call needs is that of the schedule it runs on this
- *     device: 256 bytes, except for decode-sized GEMMs (M <= 256 with at
- *     most half as many 128-row weight tiles as SMs) that split K, which also
- *     hold FP32 partials of (weight tiles x splits x M rounded up to 16, 32,
- *     64, 128 or 256) x 128 x 4 bytes.  A shape that needs more than 4 MiB is
- *     rejected with FGF8_ERR_WORKSPACE_TOO_SMALL before any launch (e.g.
- *     M = 256, N = 4096, K = 7168; M = 16 with the same N and K fits).  The
- *     4 MiB never holds the last-wave split of large GEMMs: whole tiles only.
+ *     device: the 256-byte status header for every shape (the small-M split
+ *     reduces within its thread-block cluster), so no valid shape is
+ *     rejected for its size.  (FGF8_ERR_WORKSPACE_TOO_SMALL stays the answer
+ *     should a schedule ever need more than the array.)  The array never holds
+ *     the last-wave split of large GEMMs: whole tiles only.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; each call clears the part that must start at zero (the device
- *     status word and the split-K arrival counters) on `stream` before its
- *     kernel.  Calls whose work can overlap on the GPU (different streams, no
+ *     status word and the arrival counters) on `stream` before its kernel.  Calls whose work can overlap on the GPU (different streams, no
  *     ordering between them) race on the array: order them, or use
  *     fp8_gemm_blockscaled with separate workspaces.
  *   - A device-side wait that expires leaves FGF8_ERR_TIMEOUT in the array's
@@ -305,10 +305,10 @@ fgf8_status fp8_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int6
  *   C  : [E][cap][ldc] BF16 or FP32, ldc >= N, ldc * element size % 16 == 0;
  *        rows m >= counts[e] are not written.
  *   num_experts : 0 .. 65535 (0 is a no-op that reads no pointer).
- *   workspace : at least fgf8_masked_gemm_workspace_bytes(E, cap, N, K) bytes,
- *        256-byte aligned, zero-filled before its first use (status word and
- *        one arrival counter per expert and 128 weight rows; the kernel leaves
- *        them zero).  Calls sharing a workspace must not overlap on the GPU.
+ *   workspace : at least fgf8_masked_gemm_workspace_bytes(E, cap, N, K) bytes
+ *        (256), 256-byte aligned, zero-filled before its first use (the status
+ *        word; a split of K is reduced within its thread-block cluster).
+ *        Calls sharing a workspace must not overlap on the GPU.
  */
 fgf8_status fp8_masked_grouped_gemm_blockscaled(const uint8_t *A, const float *sa, int64_t ldsa, const uint8_t *B,
                                                 const float *sb, int64_t ldsb, const int32_t *counts,

@@ -40,12 +40,15 @@ fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, 
  * fgf8_testing_gemm_schedule -- host only, launches nothing: the schedule that
  * fp8_gemm_blockscaled picks for a dense M x N x K GEMM with B scales of
  * `bkind` (0 block, 1 per row), a workspace of `ws_bytes` and `num_sms` SMs:
- *   schedule[0] = 1 if the small-M kernel runs (the rest is then 0);
+ *   schedule[0] = 1 if the small-M kernel runs (then only schedule[3] is
+ *                 set besides);
  *   schedule[1] = output tile width (128 or 256 columns);
  *   schedule[2] = tiles computed whole (a multiple of the number of
  *                 concurrent CTAs, or CTA pairs, when the last wave is
  *                 split, else all of them);
- *   schedule[3] = K pieces per remaining tile (1 = no split);
+ *   schedule[3] = K pieces per remaining tile (1 = no split); for the
+ *                 small-M kernel, the CTAs (one cluster) that split the K
+ *                 groups of each 128-row weight tile;
  *   schedule[4] = 1 if the CTA-pair kernel runs (256 x 256 tiles on two SMs;
  *                 num_sms / 2 pairs are assumed), 0 for 128-row tiles.
  * `schedule` points to 5 host int32.  Lets tests check the schedule choice on
@@ -65,6 +68,16 @@ fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t 
  * thread-safe: set it while no other thread calls the library.
  */
 fgf8_status fgf8_testing_set_pair(int32_t mode);
+
+/*
+ * fgf8_testing_set_small_splits -- 1..8: from now on, in this process, the
+ * dense small-M kernel (fp8_gemm_blockscaled with M <= 256 and block scales)
+ * splits the K groups of each weight tile over this many CTAs (at most K/128);
+ * 0: back to the planner's choice.  Results are the same sum grouped
+ * differently (within the GEMM bound).  Returns FGF8_ERR_INVALID_ARG outside
+ * 0..8.  Not thread-safe: set it while no other thread calls the library.
+ */
+fgf8_status fgf8_testing_set_small_splits(int32_t splits);
 
 /*
  * fgf8_testing_pair_clusters -- the number of CTA pairs of the pair GEMM

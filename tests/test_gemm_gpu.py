@@ -198,9 +198,11 @@ def test_pair_output_row_stride_and_untouched_padding(pair_on):
     assert_within_bound(bf16_out_to_f64(out), Cr, S)
 
 
-# M <= 256 takes the small-M path (weights on the MMA's M side, K split over
-# the SMs, last-arriving split adds the partials): every token width 16..256,
-# a ragged last weight tile, 1 to 8 splits, both output types.
+# M <= 256 takes the small-M path (weights on the MMA's M side, the K groups
+# of each weight tile split over the CTAs of a thread-block cluster, which add
+# their partials in split order through distributed shared memory): every
+# token width 16..256, a ragged last weight tile, 1 to 8 splits, both output
+# types.
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 7168), (5, 144, 2048), (33, 512, 1024), (64, 7168, 2048),
                                    (100, 400, 640), (200, 1024, 3072), (256, 2048, 512), (250, 16, 128)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
@@ -215,7 +217,7 @@ def test_small_m(M, N, K, out):
 
 
 def test_small_m_repeated_calls_same_workspace():
-    # the split-K arrival counters must be back at zero after every call
+    # the same split on every call: bit-identical outputs
     rng = np.random.default_rng(77)
     A = wl.bf16_normal(rng, (48, 1024))
     B = wl.bf16_normal(rng, (1024, 1024), 0.02)
@@ -229,8 +231,33 @@ def test_small_m_repeated_calls_same_workspace():
         assert_within_bound(bf16_out_to_f64(o), Cr, S)
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2]), "split order must be deterministic"
     assert fg.fgf8_read_status(ws) == (0, 0)
-    tickets = ws[256:256 + 8 * 4].view(torch.int32)
-    assert int(tickets.abs().sum()) == 0
+
+
+@pytest.fixture
+def small_splits():
+    yield lambda s: fg.lib().fgf8_testing_set_small_splits(s)
+    fg.lib().fgf8_testing_set_small_splits(0)
+
+
+# Every cluster size the small-M kernel can take (1..8 CTAs per weight tile,
+# odd sizes included), forced through the testing hook: each within the bound
+# against the oracle and bit-identical over repeated launches.
+@pytest.mark.parametrize("M,N,K", [(48, 1024, 2048), (200, 400, 1024)])
+def test_small_m_every_split_count(M, N, K, small_splits):
+    rng = np.random.default_rng(M + N + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (N, K), 0.02)
+    qa, sa = oracle.quant_act_1x128(A)
+    qb, sb = oracle.quant_w_128x128(B)
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb)
+    ops = [_d(qa), _d(sa), _d(qb), _d(sb)]
+    for splits in range(1, 9):
+        assert small_splits(splits) == 0
+        assert fg.fgf8_testing_gemm_schedule(M, N, K)["tail_s"] == min(splits, K // 128)
+        outs = [fg.fp8_gemm_blockscaled(*ops, check=True) for _ in range(2)]
+        assert torch.equal(outs[0], outs[1]), f"{splits} splits: repeated launches differ"
+        assert_within_bound(bf16_out_to_f64(outs[0]), Cr, S, f"{M}x{N}x{K} with {splits} splits")
+    assert small_splits(9) == 1                       # FGF8_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 256, 512), (256, 144, 384), (512, 256, 1024)])
@@ -500,8 +527,8 @@ def _run_masked(w, dt, rows=None, workspace=None):
     return g, Cg, Cr, S
 
 
-# E x weight tiles below the SM count -> K split with the ticketed reduction;
-# 40 x 4 tiles -> one split, direct stores; token widths 16, 64, 256
+# E x weight tiles below the SM count -> K split over a cluster per (expert,
+# weight tile); 40 x 4 tiles -> one split, direct stores; token widths 16, 64, 256
 @pytest.mark.parametrize("counts,cap,N,K", [([64, 5, 0, 33], 64, 256, 512), ([16, 1], 16, 128, 256),
                                             ([256, 0, 200, 17, 1, 128, 255, 64], 256, 512, 1024),
                                             ([int(c) for c in np.random.default_rng(5).integers(0, 33, 40)], 32, 512, 512)])
@@ -528,7 +555,6 @@ def test_masked_grouped_repeated_calls_same_workspace():
         for e, c in enumerate(g.counts):
             assert torch.equal(o[e, :c], outs[0][e, :c]), "split order must be deterministic"
     assert fg.fgf8_read_status(ws) == (0, 0)
-    assert int(ws[256:256 + 4 * 2 * 4].view(torch.int32).abs().sum()) == 0, "arrival counters left non-zero"
 
 
 def test_full_size_moe_decode_sampled():
@@ -585,10 +611,10 @@ def test_bf16a_row_stride_and_rejects_large_m():
         fg.fp8_gemm_bf16a_blockscaled(dev_bf16(wl.bf16_normal(rng, (257, 512))), qb, sb)
 
 
-# One workspace serves every GEMM kernel in turn: the split kernels' arrival
-# counters sit in one region that no kernel writes partial sums into, so a
-# small-M split-K call, a masked call and a last-wave split call leave each
-# other's counters at zero.  Each result is checked against the oracle.
+# One workspace serves every GEMM kernel in turn: a small-M split-K call and a
+# masked call (both reduced within their clusters) and a last-wave split call
+# (arrival counters in their own region, no partial sums written there) leave
+# the counters at zero.  Each result is checked against the oracle.
 def test_one_workspace_serves_every_kernel():
     L = fg.lib()
     need = max(L.fgf8_gemm_workspace_bytes(16, 1024, 2048, 1), L.fgf8_gemm_workspace_bytes(384, 3072, 1792, 1),
