@@ -534,7 +534,7 @@ def time_ops(path, dev, stream, reps, fp8_peak, peaks):
         g.replay()
         for e0, e1 in ev:
             flush.fill_(1.0)
-            torch.cuda._sleep(200_000)
+            torch.cuda._sleep(SLEEP_CYCLES)
             e0.record()
             g.replay()
             e1.record()
@@ -556,10 +556,10 @@ def time_ops(path, dev, stream, reps, fp8_peak, peaks):
 def time_ops_rotating(paths, dev, stream, reps, fp8_peak, peaks):
     """Per-kernel device time for workloads whose operands fit in L2: the
     same op of len(paths) independent copies of the workload (their operand
-    sets together larger than twice the 126 MB L2) captured back to back into
-    one CUDA graph, so that no launch finds its inputs in L2 and the launch
-    overhead of one graph replay is spread over len(paths) kernels; the L2 is
-    flushed before each timed replay.  Reports the mean time per launch."""
+    sets together larger than twice the 126 MB L2) captured back to back,
+    ROTATE_ROUNDS times over, into one CUDA graph, so that no launch finds its
+    inputs in L2 and the start of a replay is spread over many kernels; the L2
+    is flushed before each timed replay.  Reports the mean time per launch."""
     import torch
     flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
     R = len(paths)
@@ -571,20 +571,22 @@ def time_ops_rotating(paths, dev, stream, reps, fp8_peak, peaks):
                 pth.ops[j][2]()
             torch.cuda.synchronize(dev)
             with torch.cuda.graph(g, stream=stream):
-                for pth in paths:
-                    pth.ops[j][2]()
+                for _ in range(ROTATE_ROUNDS):
+                    for pth in paths:
+                        pth.ops[j][2]()
         torch.cuda.current_stream(dev).wait_stream(stream)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         g.replay()
         for e0, e1 in ev:
             flush.fill_(1.0)
-            torch.cuda._sleep(200_000)
+            torch.cuda._sleep(SLEEP_CYCLES)
             e0.record()
             g.replay()
             e1.record()
         torch.cuda.synchronize(dev)
-        avg = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps / R
-        entry = {"kind": kind, "ms": round(avg, 5), "timing": f"{R} back-to-back launches on separate operand copies"}
+        avg = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps / (R * ROTATE_ROUNDS)
+        entry = {"kind": kind, "ms": round(avg, 5),
+                 "timing": f"{R * ROTATE_ROUNDS} back-to-back launches on {R} separate operand copies"}
         if kind == "gemm":
             entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
             entry["frac_fp8_peak"] = round(entry["TFLOP/s"] / fp8_peak, 4)
@@ -643,6 +645,11 @@ EXTRA_WORKLOADS = ["tiny", "decode", "moe", "wgrad", "dgrad"]
 # workload's operands take ~2.8 GB, far more than twice L2.
 ROTATE_BELOW_BYTES = 126 << 20
 ROTATE_COPIES = 8
+ROTATE_ROUNDS = 4
+# A device-side sleep before each timed replay (about 1 ms at 2 GHz) keeps the
+# GPU busy while the host submits the event and the replay, so that the timed
+# interval holds the kernels alone and not the submission of the graph.
+SLEEP_CYCLES = 2_000_000
 
 
 def run_workloads(args, dev, stream, fp8_peak, peaks, version):

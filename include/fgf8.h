@@ -239,8 +239,10 @@ fgf8_status fgf8_noalloc_read_status(void *stream, int32_t *site);
  * the E4M3 copy of the tokens never goes through HBM ([why-be]
  * FP8-cast-with-TMA passage: the quantization round trip through memory, and
  * the wish to fuse the cast into the load).  The codes and scales are those
- * of fp8_quant_act_1x128 (same rule, same arithmetic), so the result equals
- * fp8_quant_act_1x128 followed by fp8_gemm_blockscaled bit for bit.
+ * of fp8_quant_act_1x128 (same rule, same arithmetic), so for M <= 128 the
+ * result equals fp8_quant_act_1x128 followed by fp8_gemm_blockscaled bit for
+ * bit; for 129 <= M <= 256 fp8_gemm_blockscaled runs large tiles, whose sum is
+ * grouped differently (both within the GEMM error bound).
  *
  *   x  : BF16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.  1 <= M <= 256.
  *   B  : E4M3 [N][K] with 128x128 block scales sb [K/128][ldsb] as in

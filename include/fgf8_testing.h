@@ -71,7 +71,7 @@ fgf8_status fgf8_testing_set_pair(int32_t mode);
 
 /*
  * fgf8_testing_set_small_splits -- 1..8: from now on, in this process, the
- * dense small-M kernel (fp8_gemm_blockscaled with M <= 256 and block scales)
+ * dense small-M kernel (fp8_gemm_blockscaled with M <= 128 and block scales)
  * splits the K groups of each weight tile over this many CTAs (at most K/128);
  * 0: back to the planner's choice.  Results are the same sum grouped
  * differently (within the GEMM bound).  Returns FGF8_ERR_INVALID_ARG outside

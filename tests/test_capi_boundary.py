@@ -261,6 +261,13 @@ def test_schedule_of_the_prefill_pair_and_wgrad(L):
     sch = fg.fgf8_testing_gemm_schedule(7168, 2048, 8192, 1)
     assert sch["bn"] == 256 and sch["dp_tiles"] == 444 and sch["tail_s"] > 1
     assert fg.fgf8_testing_gemm_schedule(16, 4096, 7168)["small_m"] == 1
+    # decode: up to 128 tokens on the small-M kernel (K over 4 CTAs per weight
+    # tile for N = 4096); 256 tokens on 64 large tiles of 128 x 128 cut into
+    # 2 K pieces (128 CTAs)
+    assert fg.fgf8_testing_gemm_schedule(128, 4096, 7168) == {"small_m": 1, "bn": 0, "dp_tiles": 0,
+                                                              "tail_s": 4, "pair": 0}
+    assert fg.fgf8_testing_gemm_schedule(256, 4096, 7168) == {"small_m": 0, "bn": 128, "dp_tiles": 0,
+                                                              "tail_s": 2, "pair": 0}
 
 
 def test_pair_schedule_of_the_prefill_pair(L, pair_on):

@@ -198,11 +198,11 @@ def test_pair_output_row_stride_and_untouched_padding(pair_on):
     assert_within_bound(bf16_out_to_f64(out), Cr, S)
 
 
-# M <= 256 takes the small-M path (weights on the MMA's M side, the K groups
+# M <= 128 takes the small-M path (weights on the MMA's M side, the K groups
 # of each weight tile split over the CTAs of a thread-block cluster, which add
 # their partials in split order through distributed shared memory): every
-# token width 16..256, a ragged last weight tile, 1 to 8 splits, both output
-# types.
+# token width 16..128, a ragged last weight tile, 1 to 8 splits, both output
+# types; 129..256 tokens (large tiles with the last-wave split) as well.
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 7168), (5, 144, 2048), (33, 512, 1024), (64, 7168, 2048),
                                    (100, 400, 640), (200, 1024, 3072), (256, 2048, 512), (250, 16, 128)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
@@ -242,7 +242,7 @@ def small_splits():
 # Every cluster size the small-M kernel can take (1..8 CTAs per weight tile,
 # odd sizes included), forced through the testing hook: each within the bound
 # against the oracle and bit-identical over repeated launches.
-@pytest.mark.parametrize("M,N,K", [(48, 1024, 2048), (200, 400, 1024)])
+@pytest.mark.parametrize("M,N,K", [(48, 1024, 2048), (100, 400, 1024)])
 def test_small_m_every_split_count(M, N, K, small_splits):
     rng = np.random.default_rng(M + N + K)
     A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
@@ -574,8 +574,11 @@ def test_full_size_moe_decode_sampled():
                                    (256, 7168, 2048), (200, 1024, 640)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
 def test_bf16a_equals_quantize_then_gemm(M, N, K, out):
-    # same rule and arithmetic as the quantization kernel: the fused GEMM must
-    # equal quantize + GEMM bit for bit, and the oracle within the bound
+    # same rule and arithmetic as the quantization kernel: up to 128 tokens
+    # (where the two-step GEMM runs the small-M kernel too) the fused GEMM
+    # must equal quantize + GEMM bit for bit; beyond, the two-step GEMM runs
+    # large tiles (the same sum grouped differently), so both are held to the
+    # bound against the oracle
     rng = np.random.default_rng(M * 11 + N + K)
     X = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
     W = wl.bf16_normal(rng, (N, K), 0.02)
@@ -587,13 +590,15 @@ def test_bf16a_equals_quantize_then_gemm(M, N, K, out):
     twostep = fg.fp8_gemm_blockscaled(qa, sa, qb, sb, out_dtype=dt)
     torch.cuda.synchronize()
     iv = torch.int16 if dt == torch.bfloat16 else torch.int32
-    assert torch.equal(fused.view(iv), twostep.view(iv)), "fused quantization differs from the two-step path"
+    if M <= 128:
+        assert torch.equal(fused.view(iv), twostep.view(iv)), "fused quantization differs from the two-step path"
     rqa, rsa = oracle.quant_act_1x128(X)
     rqb, rsb = oracle.quant_w_128x128(W)
     rows = _sample_rows(M, 16, M)
     Cr, S = oracle.gemm_blockscaled(rqa, rsa, rqb, rsb, rows=rows)
-    Cg = bf16_out_to_f64(fused) if dt == torch.bfloat16 else fused.cpu().numpy().astype(np.float64)
-    assert_within_bound(Cg[rows], Cr, S, f"bf16a {M}x{N}x{K}")
+    for C, what in ((fused, "bf16a"), (twostep, "two-step")):
+        Cg = bf16_out_to_f64(C) if dt == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
+        assert_within_bound(Cg[rows], Cr, S, f"{what} {M}x{N}x{K}")
 
 
 def test_bf16a_row_stride_and_rejects_large_m():
