@@ -427,17 +427,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + lane_addr + buf * BN + col0;
                 if constexpr (ROW_SB) {
-                    // per-column B scales: twice the FP work per element, so one
-                    // 32-column load at a time (keeps the register budget spill-free)
+                    // per-column B scales: twice the FP work per element; 64
+                    // columns per load and wait, the scales 4 at a time
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_sync<32>(taddr + c * 32, r);
+                    for (int g = 0; g < NCH / 2; ++g) {
+                        uint32_t r[64];
+                        tmem_ld_sync<64>(taddr + g * 64, r);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float2 pv = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                            const float2 sbp = *reinterpret_cast<const float2 *>(sbv + c * 32 + 2 * i);
-                            acc[c * 16 + i] = __ffma2_rn(pv, __fmul2_rn(sa2, sbp), acc[c * 16 + i]);
+                            const float4 sb4 = *reinterpret_cast<const float4 *>(sbv + g * 64 + 4 * i);
+                            const float2 p0 = make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]));
+                            const float2 p1 = make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            acc[g * 32 + 2 * i] = __ffma2_rn(p0, __fmul2_rn(sa2, make_float2(sb4.x, sb4.y)),
+                                                             acc[g * 32 + 2 * i]);
+                            acc[g * 32 + 2 * i + 1] = __ffma2_rn(p1, __fmul2_rn(sa2, make_float2(sb4.z, sb4.w)),
+                                                                 acc[g * 32 + 2 * i + 1]);
                         }
                     }
                 } else {
