@@ -44,6 +44,10 @@ FUSED_A_MAX_M = 256         # token count up to which fp8_gemm_bf16a_blockscaled
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
+    "fgf8 0.10 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md
+        "prefill_pair_4096x18432x7168/up.gemm": 167797760 + 126922240,
+        "prefill_pair_4096x18432x7168/down.gemm": 522013696 + 51453184,
+    },
     "fgf8 0.9 sm_103a": {                                    # profiles/gemm_blockscaled_prefill_traffic.md
         "prefill_pair_4096x18432x7168/up.gemm": 166803456 + 126609152,
         "prefill_pair_4096x18432x7168/down.gemm": 521767168 + 51166720,
@@ -689,6 +693,8 @@ def run_workloads(args, dev, stream, fp8_peak, peaks, version):
         out[key] = {"kernels": per_op, "ms_sum_of_kernels": round(ms, 4),
                     "gemm_GFLOP": round(gflop, 3), "TFLOP/s_over_kernels": round(gflop / ms, 1),
                     "roofline": roofline_of(path, per_op, work.name, fp8_peak, peaks, version)}
+        if not args.no_cpu_baseline and not variant:
+            out[key]["oracle"] = workload_oracle(work, args)
         del path, work
         torch.cuda.empty_cache()
     return out
@@ -759,54 +765,122 @@ def _quant_slices(pool, fn, x, threads, axis):
 def oracle_sample(work, rows, threads, seed=0):
     """The oracle as it stands (plain C in binary64, called through ctypes,
     which releases the GIL, so `threads` host threads run it side by side) on
-    each dense GEMM of the workload: every operand of the step quantized in
-    full (A 1x128, B 128x128, in slices of 128 rows or columns spread over the
-    threads), and `rows` seeded rows of the output against all N columns (the
-    rows split over the threads).  Returns (GEMM FLOPs of the sample, measured
-    seconds, seconds of the whole step extrapolated from it: the GEMM part
-    scaled by M / rows)."""
+    each GEMM of the workload: every operand quantized in full (in slices of
+    128 rows or columns spread over the threads) as the device path quantizes
+    it (A 1x128 and B 128x128; W^T for dgrad; both operands 128x1 along the
+    tokens for wgrad; per expert for the grouped and masked layouts), and
+    `rows` seeded output rows against all N columns (grouped: a quarter of
+    that, at least one, of every expert with tokens; masked: that many rows
+    of every live expert),
+    the rows split over the threads.  Returns (GEMM FLOPs of the sample,
+    measured seconds, seconds of the whole workload extrapolated from it: the
+    GEMM part scaled by the real output rows / the sampled rows)."""
     from concurrent.futures import ThreadPoolExecutor
     import oracle
-    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad
+    from fine_grained_fp8_weight_b300.workloads import Dense, Dgrad, Grouped, Masked, Wgrad
     oracle.lib()                                 # built and loaded before the threads start
     flops = secs = full = 0.0
     rng = np.random.default_rng(seed)
+
+    def quant_rows(pool, fn, x, axis=0):
+        # fn over 128-row (axis 0) or 128-column (axis 1) slices; codes and scales reassembled
+        parts, cuts = _quant_slices(pool, fn, x, threads, axis)
+        return parts, cuts
+
+    def act_1x128(pool, A):
+        M, K = A.shape
+        parts, cuts = quant_rows(pool, oracle.quant_act_1x128, A)
+        sa = np.zeros((K // 128, (M + 3) // 4 * 4), np.float32)
+        for (r0, r1), (_, s_) in zip(cuts, parts):
+            sa[:, r0:r1] = s_[:, :r1 - r0]
+        return np.concatenate([q for q, _ in parts]), sa
+
+    def w_128x128(pool, Bw):
+        N, K = Bw.shape
+        parts, cuts = quant_rows(pool, oracle.quant_w_128x128, Bw)
+        sb = np.zeros((K // 128, ((N + 127) // 128 + 3) // 4 * 4), np.float32)
+        for (b0, b1), (_, s_) in zip(cuts, parts):
+            sb[:, b0 // 128:(b1 + 127) // 128] = s_[:, :(b1 - b0 + 127) // 128]
+        return np.concatenate([q for q, _ in parts]), sb
+
+    def act_128x1(pool, X):
+        # transposed output of 128x1 tiles along the tokens: qT [K, T], per-row
+        # scales of qT as the GEMM reads them, sb[t/128][k]
+        T, K = X.shape
+        parts, cuts = quant_rows(pool, oracle.quant_act_128x1, X)
+        qT = np.concatenate([q for q, _ in parts], axis=1)
+        sT = np.concatenate([s_ for _, s_ in parts], axis=0)
+        return qT, np.ascontiguousarray(sT[:, :(K + 3) // 4 * 4])
+
     with ThreadPoolExecutor(max_workers=threads) as pool:
         for g in work.gemms:
-            if isinstance(g, Dense):
-                A, Bw = g.A, g.B
-            elif isinstance(g, Dgrad):
-                A, Bw = g.dY, g.W
+            t0 = time.perf_counter()
+            if isinstance(g, (Dense, Dgrad)):
+                A = g.A if isinstance(g, Dense) else g.dY
+                qa, sa = act_1x128(pool, A)
+                if isinstance(g, Dense):
+                    qb, sb = w_128x128(pool, g.B)
+                else:                            # B = W^T: slices of W's columns are rows of W^T
+                    Bw = g.W
+                    N = Bw.shape[1]
+                    parts, cuts = quant_rows(pool, oracle.quant_w_128x128_t, Bw, axis=1)
+                    sb = np.zeros((A.shape[1] // 128, (N // 128 + 3) // 4 * 4), np.float32)
+                    for (c0, c1), (_, s_) in zip(cuts, parts):
+                        sb[:, c0 // 128:c1 // 128] = s_[:, :(c1 - c0) // 128]
+                    qb = np.concatenate([q for q, _ in parts])
+                t1 = time.perf_counter()
+                M, K = qa.shape
+                N = qb.shape[0]
+                r = np.sort(rng.choice(M, size=min(rows, M), replace=False))
+                chunks = [c for c in np.array_split(r, threads) if len(c)]
+                list(pool.map(lambda c: oracle.gemm_blockscaled(qa, sa, qb, sb, 0, rows=c), chunks))
+                real_rows = M
+            elif isinstance(g, Wgrad):
+                qa, sa = act_128x1(pool, g.dY)   # dY^T [N, T], scales per (token group, row)
+                qb, sb = act_128x1(pool, g.X)    # X^T [K, T]
+                t1 = time.perf_counter()
+                M, K = qa.shape
+                N = qb.shape[0]
+                r = np.sort(rng.choice(M, size=min(rows, M), replace=False))
+                chunks = [c for c in np.array_split(r, threads) if len(c)]
+                list(pool.map(lambda c: oracle.gemm_blockscaled(qa, sa, qb, sb, 1, rows=c), chunks))
+                real_rows = M
+            elif isinstance(g, Grouped):
+                qa, sa = act_1x128(pool, g.A)
+                E, N, K = g.B.shape
+                qs = list(pool.map(oracle.quant_w_128x128, [g.B[e] for e in range(E)]))
+                qb = np.stack([q for q, _ in qs])
+                sb = np.stack([s_ for _, s_ in qs])
+                t1 = time.perf_counter()
+                starts = np.concatenate([[0], np.cumsum((g.counts + 127) // 128 * 128)])
+                per_e = max(1, rows // 4)        # 32 experts: a quarter of the rows each
+                r = np.sort(np.concatenate([starts[e] + rng.choice(int(g.counts[e]), size=min(per_e, int(g.counts[e])),
+                                                                   replace=False)
+                                            for e in range(E) if g.counts[e] > 0]))
+                chunks = [c for c in np.array_split(r, threads) if len(c)]
+                list(pool.map(lambda c: oracle.grouped_gemm_blockscaled(qa, sa, qb, sb, g.m_indices, rows=c), chunks))
+                real_rows = int(g.counts.sum())
+            elif isinstance(g, Masked):
+                E, cap, K = g.A.shape
+                qa, sa = act_1x128(pool, g.A.reshape(E * cap, K))
+                N = g.B.shape[1]
+                live = [e for e in range(E) if g.counts[e] > 0]
+                qs = dict(zip(live, pool.map(oracle.quant_w_128x128, [g.B[e] for e in live])))
+                t1 = time.perf_counter()
+                jobs = [(e, np.sort(rng.choice(int(g.counts[e]), size=min(rows, int(g.counts[e])), replace=False)))
+                        for e in live]
+                list(pool.map(lambda j: oracle.gemm_blockscaled(
+                    qa[j[0] * cap:j[0] * cap + int(g.counts[j[0]])],
+                    np.ascontiguousarray(sa[:, j[0] * cap:(j[0] + 1) * cap]), qs[j[0]][0], qs[j[0]][1], 0,
+                    rows=j[1]), jobs))
+                r = np.concatenate([j[1] for j in jobs])
+                real_rows = int(g.counts.sum())
             else:
                 continue
-            M, K = A.shape
-            t0 = time.perf_counter()
-            parts, cuts = _quant_slices(pool, oracle.quant_act_1x128, A, threads, 0)
-            qa = np.concatenate([q for q, _ in parts])
-            sa = np.zeros((K // 128, (M + 3) // 4 * 4), np.float32)
-            for (r0, r1), (_, s_) in zip(cuts, parts):
-                sa[:, r0:r1] = s_[:, :r1 - r0]
-            if isinstance(g, Dense):
-                N = Bw.shape[0]
-                parts, cuts = _quant_slices(pool, oracle.quant_w_128x128, Bw, threads, 0)
-                sb = np.zeros((K // 128, ((N + 127) // 128 + 3) // 4 * 4), np.float32)
-                for (b0, b1), (_, s_) in zip(cuts, parts):
-                    sb[:, b0 // 128:(b1 + 127) // 128] = s_[:, :(b1 - b0 + 127) // 128]
-            else:                                # B = W^T: slices of W's columns are rows of W^T
-                N = Bw.shape[1]
-                parts, cuts = _quant_slices(pool, oracle.quant_w_128x128_t, Bw, threads, 1)
-                sb = np.zeros((K // 128, (N // 128 + 3) // 4 * 4), np.float32)
-                for (c0, c1), (_, s_) in zip(cuts, parts):
-                    sb[:, c0 // 128:c1 // 128] = s_[:, :(c1 - c0) // 128]
-            qb = np.concatenate([q for q, _ in parts])
-            t1 = time.perf_counter()
-            r = np.sort(rng.choice(M, size=min(rows, M), replace=False))
-            chunks = [c for c in np.array_split(r, threads) if len(c)]
-            list(pool.map(lambda c: oracle.gemm_blockscaled(qa, sa, qb, sb, 0, rows=c), chunks))
             t2 = time.perf_counter()
             flops += 2.0 * len(r) * N * K
             secs += t2 - t0
-            full += (t1 - t0) + (t2 - t1) * (M / len(r))
+            full += (t1 - t0) + (t2 - t1) * (real_rows / len(r))
     return flops, secs, full
 
 
@@ -832,6 +906,20 @@ def cpu_baseline(work, args):
                       f"{args.cpu_rows} seeded rows of each GEMM's output against all N in binary64); plain C "
                       f"oracle on {threads} host threads; the full step's time is extrapolated from it "
                       f"(GEMM part x M/rows)"}
+
+
+def workload_oracle(work, args):
+    """The oracle on the host cores for one workload of the workloads key:
+    one sample (every operand quantized in full, args.cpu_rows seeded output
+    rows of each GEMM -- of each expert for the grouped layouts -- against all
+    N), its measured seconds and the workload's time extrapolated from it."""
+    threads = _cores()
+    f, d, fu = oracle_sample(work, args.cpu_rows, threads, seed=7)
+    return {"GFLOP/s": round(f / d / 1e9, 4), "seconds": round(d, 2), "cores": threads, "kind": "oracle",
+            "workload_seconds_extrapolated": round(fu, 1),
+            "sample": f"every operand quantized in full and {args.cpu_rows} seeded output rows of each GEMM "
+                      f"(per live expert for the masked layout, {max(1, args.cpu_rows // 4)} per expert for the "
+                      f"grouped one) against all N, binary64, {threads} host threads"}
 
 
 def run_reference(args, rank, world):
