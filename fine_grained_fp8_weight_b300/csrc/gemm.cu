@@ -388,6 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row = quarter * 32 + lane;
         const uint32_t lane_addr = (quarter * 32) << 16;
         const uint32_t col0 = half * HALF;
+        // Per-row B scales: the partial is read in the 16x256b shape, so a
+        // thread holds 4 rows x HALF/4 columns (instead of 1 row x HALF) and
+        // reads a quarter of the column scales.  acc[a], a = (j*NREP + i)*2 + k:
+        // row quarter*32 + 16j + 8k + lane/4, columns col0 + 8i + 2(lane%4), +1.
+        constexpr int NREP = HALF / 8;
+        const uint32_t rs_r = quarter * 32 + (lane >> 2);
+        const uint32_t rs_c = col0 + 2 * (lane & 3);
         uint32_t it = 0;                                    // K groups so far (TMEM buffers)
         uint32_t nslot = 0;                                 // scale slots so far
         bool ok = true;
@@ -412,11 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t g = slot * SG + pos;
-                const float sa_v = sm_sa[g * BM + row];
-                const float *sbv = sm_sb + g * L::sb_pitch + (ROW_SB ? col0 : 0);
-                const float blk = ROW_SB ? 0.0f : sa_v * sm_sb[g * L::sb_pitch + sb_sel];
+                const float blk = ROW_SB ? 0.0f : sm_sa[g * BM + row] * sm_sb[g * L::sb_pitch + sb_sel];
                 const float2 blk2 = make_float2(blk, blk);
-                const float2 sa2 = make_float2(sa_v, sa_v);
                 const uint32_t buf = it & 1, phb = (it >> 1) & 1;
                 if (!mbar_wait(&tm_full[buf], phb, abort_flag)) {
                     record_timeout(p.status, kSiteEpiTmemFull);
@@ -427,21 +431,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + lane_addr + buf * BN + col0;
                 if constexpr (ROW_SB) {
-                    // per-column B scales: twice the FP work per element; 64
-                    // columns per load and wait, the scales 4 at a time
+                    // per-column B scales: the scales of this thread's 4 rows,
+                    // then per 8 column blocks their B scales (one pair each)
+                    // and the two 16-lane loads
+                    float sa_r[4];
 #pragma unroll
-                    for (int g = 0; g < NCH / 2; ++g) {
-                        uint32_t r[64];
-                        tmem_ld_sync<64>(taddr + g * 64, r);
+                    for (int jk = 0; jk < 4; ++jk) sa_r[jk] = sm_sa[g * BM + rs_r + 16 * (jk >> 1) + 8 * (jk & 1)];
+                    const float *sbc = sm_sb + g * L::sb_pitch + rs_c;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float4 sb4 = *reinterpret_cast<const float4 *>(sbv + g * 64 + 4 * i);
-                            const float2 p0 = make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]));
-                            const float2 p1 = make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-                            acc[g * 32 + 2 * i] = __ffma2_rn(p0, __fmul2_rn(sa2, make_float2(sb4.x, sb4.y)),
-                                                             acc[g * 32 + 2 * i]);
-                            acc[g * 32 + 2 * i + 1] = __ffma2_rn(p1, __fmul2_rn(sa2, make_float2(sb4.z, sb4.w)),
-                                                                 acc[g * 32 + 2 * i + 1]);
+                    for (int i0 = 0; i0 < NREP; i0 += 8) {
+                        // both 16-lane halves of 8 column blocks, then each
+                        // column pair's B scale once for the thread's 4 rows
+                        uint32_t r0[32], r1[32];
+                        tmem_ld_16x256b_x8_sync(tmem_base + ((quarter * 32) << 16) + buf * BN + col0 + 8 * i0, r0);
+                        tmem_ld_16x256b_x8_sync(tmem_base + ((quarter * 32 + 16) << 16) + buf * BN + col0 + 8 * i0, r1);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float2 sb2 = *reinterpret_cast<const float2 *>(sbc + 8 * (i0 + i));
+                            const int a0 = (i0 + i) * 2, a1 = (NREP + i0 + i) * 2;
+                            acc[a0] = __ffma2_rn(make_float2(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1])),
+                                                 __fmul2_rn(make_float2(sa_r[0], sa_r[0]), sb2), acc[a0]);
+                            acc[a0 + 1] = __ffma2_rn(make_float2(__uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3])),
+                                                     __fmul2_rn(make_float2(sa_r[1], sa_r[1]), sb2), acc[a0 + 1]);
+                            acc[a1] = __ffma2_rn(make_float2(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1])),
+                                                 __fmul2_rn(make_float2(sa_r[2], sa_r[2]), sb2), acc[a1]);
+                            acc[a1 + 1] = __ffma2_rn(make_float2(__uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3])),
+                                                     __fmul2_rn(make_float2(sa_r[3], sa_r[3]), sb2), acc[a1 + 1]);
                         }
                     }
                 } else {
@@ -471,10 +486,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t ti = tile - p.dp_tiles;
                 if (ok) {
                     float *mine = p.tail_partials + (int64_t)(ti * p.tail_s + piece) * (BM * BN);
+                    if constexpr (ROW_SB) {
 #pragma unroll
-                    for (int c = 0; c < HALF; c += 4)
-                        *reinterpret_cast<float4 *>(mine + ((int64_t)((col0 + c) / 4) * BM + row) * 4) =
-                            make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
+                        for (int a = 0; a < HALF / 2; ++a) {
+                            const uint32_t rr = rs_r + 16 * (a / (2 * NREP)) + 8 * (a & 1);
+                            const uint32_t cc = rs_c + 8 * ((a / 2) % NREP);
+                            *reinterpret_cast<float2 *>(mine + ((int64_t)(cc / 4) * BM + rr) * 4 + (cc & 3)) = acc[a];
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < HALF; c += 4)
+                            *reinterpret_cast<float4 *>(mine + ((int64_t)((col0 + c) / 4) * BM + row) * 4) =
+                                make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
+                    }
                 }
                 __threadfence();
                 const bool all_ok = named_barrier_and(1, kEpiWarps * 32, ok && !*abort_flag);
@@ -489,24 +513,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!all_ok || !*tail_last) continue;
                 __threadfence();
                 const float *part = p.tail_partials + (int64_t)ti * p.tail_s * (BM * BN);
+                if constexpr (ROW_SB) {
+                    // in K order, 8 values of one piece in flight at a time
+                    // (keeps the 128 accumulator registers clear of spills)
 #pragma unroll
-                for (int c = 0; c < HALF; c += 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + ((int64_t)((col0 + c) / 4) * BM + row) * 4));
-                    acc[c / 2] = make_float2(v.x, v.y);
-                    acc[c / 2 + 1] = make_float2(v.z, v.w);
-                }
-                for (int32_t q = 1; q < p.tail_s; ++q) {
-                    const float *pq = part + (int64_t)q * (BM * BN);
+                    for (int a = 0; a < HALF / 2; ++a) acc[a] = make_float2(0.0f, 0.0f);
+                    for (int32_t q = 0; q < p.tail_s; ++q) {
+                        const float *pq = part + (int64_t)q * (BM * BN);
+#pragma unroll
+                        for (int a0 = 0; a0 < HALF / 2; a0 += 8) {
+                            float2 v[8];
+#pragma unroll
+                            for (int a = a0; a < a0 + 8; ++a) {
+                                const uint32_t rr = rs_r + 16 * (a / (2 * NREP)) + 8 * (a & 1);
+                                const uint32_t cc = rs_c + 8 * ((a / 2) % NREP);
+                                v[a - a0] = __ldcg(reinterpret_cast<const float2 *>(pq + ((int64_t)(cc / 4) * BM + rr) * 4 + (cc & 3)));
+                            }
+#pragma unroll
+                            for (int a = a0; a < a0 + 8; ++a) {
+                                acc[a].x += v[a - a0].x;
+                                acc[a].y += v[a - a0].y;
+                            }
+                        }
+                    }
+                } else {
 #pragma unroll
                     for (int c = 0; c < HALF; c += 4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pq + ((int64_t)((col0 + c) / 4) * BM + row) * 4));
-                        acc[c / 2].x += v.x;
-                        acc[c / 2].y += v.y;
-                        acc[c / 2 + 1].x += v.z;
-                        acc[c / 2 + 1].y += v.w;
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part + ((int64_t)((col0 + c) / 4) * BM + row) * 4));
+                        acc[c / 2] = make_float2(v.x, v.y);
+                        acc[c / 2 + 1] = make_float2(v.z, v.w);
+                    }
+                    for (int32_t q = 1; q < p.tail_s; ++q) {
+                        const float *pq = part + (int64_t)q * (BM * BN);
+#pragma unroll
+                        for (int c = 0; c < HALF; c += 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(pq + ((int64_t)((col0 + c) / 4) * BM + row) * 4));
+                            acc[c / 2].x += v.x;
+                            acc[c / 2].y += v.y;
+                            acc[c / 2 + 1].x += v.z;
+                            acc[c / 2 + 1].y += v.w;
+                        }
                     }
                 }
             } else if (!ok) {
+                continue;
+            }
+            if constexpr (ROW_SB) {
+                // this thread's 4 rows x HALF/4 columns, a pair of columns per store
+#pragma unroll
+                for (int a = 0; a < HALF / 2; ++a) {
+                    const int64_t m = (int64_t)mb * BM + rs_r + 16 * (a / (2 * NREP)) + 8 * (a & 1);
+                    const int64_t n = (int64_t)nb * BN + rs_c + 8 * ((a / 2) % NREP);
+                    bool write = m < p.M && n < p.N;
+                    if (write && p.m_indices) write = __ldg(p.m_indices + m) >= 0;
+                    if (!write) continue;
+                    if (OUT_F32)
+                        *reinterpret_cast<float2 *>(static_cast<float *>(p.C) + m * p.ldc + n) = acc[a];
+                    else
+                        *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.C) + m * p.ldc + n) =
+                            __float22bfloat162_rn(acc[a]);
+                }
                 continue;
             }
             // write this thread's finished row segment

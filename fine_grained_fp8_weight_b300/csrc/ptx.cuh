@@ -253,6 +253,26 @@ __device__ __forceinline__ void tmem_ld_sync<64>(uint32_t taddr, uint32_t (&r)[6
         : "memory");
 }
 
+// 16 lanes x 64 columns in the 16x256b shape, and the wait, in one asm
+// statement: thread t receives, for each 8-column block i (i = 0..7), lane
+// base + t/4 at columns 8i + 2(t%4) and +1 in r[4i], r[4i+1], and lane
+// base + 8 + t/4 at the same columns in r[4i+2], r[4i+3].
+__device__ __forceinline__ void tmem_ld_16x256b_x8_sync(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31"
+        "}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_increase()
