@@ -19,3 +19,16 @@ def test_reference_arm_prints_one_json_line():
                 "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["value"] > 0
+
+
+def test_oracle_sample_covers_every_gemm_kind():
+    # the host-side oracle timing of bench.py's workloads key runs on every
+    # GEMM layout of the path (small shapes of each) and counts its work
+    sys.path.insert(0, ROOT)
+    import bench
+    from fine_grained_fp8_weight_b300 import workloads as wl
+    works = [wl.tiny(), wl.grouped_small(1, [130, 0, 7], 256, 256), wl.wgrad(2, T=256, N=256, K=128),
+             wl.dgrad(3, T=128, N=256, K=256), wl.masked_small(4, [5, 0, 16], 16, 256, 256)]
+    for w in works:
+        flops, secs, full = bench.oracle_sample(w, 3, 2, seed=0)
+        assert flops > 0 and secs > 0 and full >= secs * 0.5, w.name
