@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kActWarps * 32)
 // ------------------------------------------------------------------------
 constexpr int kTileThreads = 256;
 
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, 4)
     quant_act_tile_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
                           uint8_t *__restrict__ q, float *__restrict__ s, int64_t lds,
                           uint8_t *__restrict__ qT, float *__restrict__ sT, int64_t ldsT)
