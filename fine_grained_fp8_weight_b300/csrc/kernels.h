@@ -49,9 +49,10 @@ struct GemmArgs {
 
 // Workspace layout, the same for every GEMM kernel so that one workspace can
 // serve all of them in turn: [0, 256) status word; [256, 1280) 256 arrival
-// counters, written by nothing but the split kernels' atomics and their
-// resets to zero (small-M split-K: one per 128 weight rows and expert; the
-// last-wave split: one per tail tile); from 1280 on, FP32 partial sums.
+// counters, written by nothing but the last-wave split's atomics and their
+// resets to zero (one per tail tile); from 1280 on, its FP32 partial sums.
+// The small-M kernel's K split is reduced within a thread-block cluster and
+// needs the status word only.
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kMaxCounters = 256;
 constexpr size_t kWsPartialsOffset = kWsHeaderBytes + kMaxCounters * 4;
@@ -61,11 +62,11 @@ constexpr size_t kWsPartialsOffset = kWsHeaderBytes + kMaxCounters * 4;
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts, int num_sms);
 size_t gemm_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
 // Leading part of the workspace that must be zero when a call starts (the
-// status word and the split-K arrival counters).
+// status word and the arrival counters).
 size_t gemm_workspace_zeroed_bytes(int64_t M, int64_t N, int64_t K, int32_t num_experts);
-// The schedule launch_gemm picks: small-M kernel, or tile width, whole-tile
-// count and pieces per last-wave tile (1: no split); pair = 1 for the CTA-pair
-// kernel (256 x 256 tiles, bn = 256).
+// The schedule launch_gemm picks: small-M kernel (tail_s = its K split), or
+// tile width, whole-tile count and pieces per last-wave tile (1: no split);
+// pair = 1 for the CTA-pair kernel (256 x 128 tiles on two SMs).
 struct GemmSchedule {
     int small_m, bn, dp_tiles, tail_s, pair;
 };
@@ -73,13 +74,15 @@ GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms);
 // 1: dense block-scaled GEMMs of more than 128 rows run on CTA pairs; 0: the
 // planner's choice (single-SM tiles).  Process-wide, for tests.
 void set_pair_mode(int mode);
+// 1..8: the dense small-M kernel splits K over this many CTAs (at most K/128);
+// 0: the planner's choice.  Process-wide, for tests.
 void set_small_splits(int s);
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms);
 // Workspace bytes the schedule launch_gemm picks for `a` (with a.ws_bytes of
-// workspace) reads and writes: the status header, plus the split kernels'
+// workspace) reads and writes: the status header, plus the last-wave split's
 // counters and partials when it splits.
 size_t gemm_required_bytes(const GemmArgs &a, int num_sms);
-// CTA-pair kernel (gemm_pair.cu): 256 x 256 tiles on two SMs whose tensor
+// CTA-pair kernel (gemm_pair.cu): 256 x 128 tiles on two SMs whose tensor
 // cores run as one.  pair_max_clusters() is the number of co-resident pairs on
 // the current device (0: not available); pair_plan the tile count and the
 // last-wave split for `clusters` pairs; launch_pair returns
