@@ -49,7 +49,7 @@ fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, 
  *   schedule[3] = K pieces per remaining tile (1 = no split); for the
  *                 small-M kernel, the CTAs (one cluster) that split the K
  *                 groups of each 128-row weight tile;
- *   schedule[4] = 1 if the CTA-pair kernel runs (256 x 256 tiles on two SMs;
+ *   schedule[4] = 1 if the CTA-pair kernel runs (256 x 128 tiles on two SMs;
  *                 num_sms / 2 pairs are assumed), 0 for 128-row tiles.
  * `schedule` points to 5 host int32.  Lets tests check the schedule choice on
  * a CPU and confirm that a GPU case covers the path it is meant to.
