@@ -9,6 +9,14 @@ from fine_grained_fp8_weight_b300 import workloads as wl
 
 DEV = "cuda:0"
 
+# (label, max, mean, elements) of |C - C_ref| / S per full-size configuration,
+# printed in the test session's summary
+MARGINS = []
+
+
+def report_margin(label: str, margin, n: int):
+    MARGINS.append((label, margin[0], margin[1], int(n)))
+
 
 def ensure_built():
     fgbuild.build()
