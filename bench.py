@@ -524,7 +524,7 @@ def run_device(args, rank, world, local_rank):
 
 def time_ops(path, dev, stream, reps, fp8_peak, peaks):
     """Per-kernel device time: each op captured alone into a CUDA graph and
-    replayed, one event pair per replay, with an untimed write of a buffer
+    replayed, one event pair per replay (the median is reported), with an untimed write of a buffer
     larger than L2 in between so that no op reads inputs left in L2 by its
     previous replay.  A short device-side sleep before the first event keeps
     the GPU busy while the host submits the event and the replay, so the
@@ -549,8 +549,8 @@ def time_ops(path, dev, stream, reps, fp8_peak, peaks):
             g.replay()
             e1.record()
         torch.cuda.synchronize(dev)
-        avg = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps
-        entry = {"kind": kind, "ms": round(avg, 4)}
+        avg = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        entry = {"kind": kind, "ms": round(avg, 4), "timing": f"median of {reps} replays"}
         if kind == "gemm":
             entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
             entry["frac_fp8_peak"] = round(entry["TFLOP/s"] / fp8_peak, 4)
@@ -594,9 +594,10 @@ def time_ops_rotating(paths, dev, stream, reps, fp8_peak, peaks):
             g.replay()
             e1.record()
         torch.cuda.synchronize(dev)
-        avg = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps / (R * ROTATE_ROUNDS)
+        avg = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) / (R * ROTATE_ROUNDS)
         entry = {"kind": kind, "ms": round(avg, 5),
-                 "timing": f"{R * ROTATE_ROUNDS} back-to-back launches on {R} separate operand copies"}
+                 "timing": f"median of {reps} replays of {R * ROTATE_ROUNDS} back-to-back launches on {R} "
+                           f"separate operand copies"}
         if kind == "gemm":
             entry["TFLOP/s"] = round(work_units / (avg * 1e-3) / 1e12, 1)
             entry["frac_fp8_peak"] = round(entry["TFLOP/s"] / fp8_peak, 4)
