@@ -1371,11 +1371,6 @@ size_t masked_workspace_bytes(int32_t, int64_t, int64_t, int64_t)
     return kWsHeaderBytes;
 }
 
-size_t masked_workspace_zeroed_bytes(int32_t, int64_t)
-{
-    return kWsPartialsOffset;
-}
-
 size_t gemm_workspace_zeroed_bytes(int64_t, int64_t, int64_t, int32_t)
 {
     // status word and the arrival counters

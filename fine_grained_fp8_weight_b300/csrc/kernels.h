@@ -96,9 +96,8 @@ int pair_tile_n();          // output columns of a pair tile (128 or 256)
 size_t pair_tail_workspace_bytes();
 PairPlan pair_plan(const GemmArgs &a, int clusters);
 cudaError_t launch_pair(const GemmArgs &a, cudaStream_t stream);
-// Masked grouped layout: scratch size, its zero-initialised prefix, launch.
+// Masked grouped layout: scratch size, launch.
 size_t masked_workspace_bytes(int32_t num_experts, int64_t cap, int64_t N, int64_t K);
-size_t masked_workspace_zeroed_bytes(int32_t num_experts, int64_t N);
 cudaError_t launch_masked(const GemmArgs &a, cudaStream_t stream, int num_sms);
 // Token operand given as BF16 and quantized in the GEMM's producer (M <= 256).
 cudaError_t launch_bf16a(const GemmArgs &a, cudaStream_t stream, int num_sms);
