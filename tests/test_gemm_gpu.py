@@ -41,7 +41,7 @@ def _run_dense(Abits, Bbits, out_dtype, rows=None, bkind=0, workspace=None):
     else:
         qb, sb = oracle.quant_act_1x128(Bbits)          # per-row (1x128) B scales
     C = fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), bkind=bkind, out_dtype=out_dtype,
-                                workspace=workspace)
+                                workspace=workspace, check=True)
     torch.cuda.synchronize()
     Cg = bf16_out_to_f64(C) if out_dtype == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
     Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb, bkind, rows=rows)
@@ -311,7 +311,7 @@ def _grouped_case(seed, counts, N, K, rows=None):
     qb = np.stack(qbs)
     sb = np.stack(sbs)
     out = torch.full((w.A.shape[0], N), float("nan"), dtype=torch.bfloat16, device=DEV)
-    fg.fp8_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), _d(w.m_indices), out=out)
+    fg.fp8_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), _d(w.m_indices), out=out, check=True)
     torch.cuda.synchronize()
     Cr, S = oracle.grouped_gemm_blockscaled(qa, sa, qb, sb, w.m_indices, rows=rows)
     Cg = bf16_out_to_f64(out)
@@ -525,7 +525,8 @@ def _run_masked(w, dt, rows=None, workspace=None):
     N = qb.shape[1]
     out = torch.full((E, cap, N), float("nan"), dtype=dt, device=DEV)
     counts = torch.from_numpy(g.counts).to(DEV)
-    fg.fp8_masked_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), counts, out=out, workspace=workspace)
+    fg.fp8_masked_grouped_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), counts, out=out, workspace=workspace,
+                                           check=True)
     torch.cuda.synchronize()
     Cr, S = oracle.masked_grouped_gemm_blockscaled(qa, sa, qb, sb, g.counts, rows_per_expert=rows)
     Cg = out.float().cpu().numpy().astype(np.float64) if dt == torch.float32 else bf16_out_to_f64(out.reshape(E * cap, N)).reshape(E, cap, N)
@@ -590,7 +591,7 @@ def test_bf16a_equals_quantize_then_gemm(M, N, K, out):
     qb, sb = fg.fp8_quant_w_128x128(dev_bf16(W))
     x = dev_bf16(X)
     dt = torch.bfloat16 if out == "bf16" else torch.float32
-    fused = fg.fp8_gemm_bf16a_blockscaled(x, qb, sb, out_dtype=dt)
+    fused = fg.fp8_gemm_bf16a_blockscaled(x, qb, sb, out_dtype=dt, check=True)
     qa, sa, _, _ = fg.fp8_quant_act_1x128(x)
     twostep = fg.fp8_gemm_blockscaled(qa, sa, qb, sb, out_dtype=dt)
     torch.cuda.synchronize()
