@@ -292,3 +292,23 @@ def test_schedule_rejects(L):
     assert f(128, 128, 128, 2, 1 << 20, 148, out) == 1
     assert f(128, 128, 128, 0, 1 << 20, 0, out) == 1
     assert f(128, 128, 128, 0, 1 << 20, 148, None) == 1
+
+
+def test_small_m_cluster_sizes(L):
+    """The small-M kernel's K split is one thread-block cluster per weight tile:
+    at most 8 CTAs (the portable cluster size), at most K/128, and all
+    clusters fit one wave of the SMs."""
+    seen = set()
+    for M in (1, 16, 33, 64, 128):
+        for N in (16, 128, 256, 1024, 2048, 4096, 7168, 9472):
+            for K in (128, 256, 512, 2048, 7168, 18432):
+                sch = fg.fgf8_testing_gemm_schedule(M, N, K)
+                if not sch["small_m"]:
+                    assert N > 74 * 128
+                    continue
+                S = sch["tail_s"]
+                tiles = (N + 127) // 128
+                assert 1 <= S <= min(8, K // 128), (M, N, K, S)
+                assert tiles * S <= 148, (M, N, K, S)
+                seen.add(S)
+    assert seen >= {1, 2, 4, 8}
