@@ -44,6 +44,11 @@ FUSED_A_MAX_M = 256         # token count up to which fp8_gemm_bf16a_blockscaled
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
+    # 0.12 changed the masked-layout small-M launch only: the prefill GEMMs run the 0.10 kernel
+    "fgf8 0.12 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md
+        "prefill_pair_4096x18432x7168/up.gemm": 167797760 + 126922240,
+        "prefill_pair_4096x18432x7168/down.gemm": 522013696 + 51453184,
+    },
     # 0.11 changed the per-row-B promotion only: the prefill GEMMs (block B scales) run the
     # 0.10 kernel unchanged
     "fgf8 0.11 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md

@@ -75,7 +75,7 @@ const char *fgf8_status_string(fgf8_status st)
 
 const char *fgf8_version(void)
 {
-    return "fgf8 0.11 sm_103a";
+    return "fgf8 0.12 sm_103a";
 }
 
 fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,

@@ -643,17 +643,21 @@ struct SmallParams {
     int64_t ldsb;
 };
 
-// Shared memory of the small-M kernel.  Work goes in batches of GB K groups:
-// one stage holds the weight and token tiles of GB groups (one barrier
-// handshake per batch), one scale slot their scales, one TMEM buffer their GB
-// partials side by side (GB * NT columns).
+// Shared memory of the small-M kernel.  Work goes in batches of up to GB K
+// groups: one stage holds the weight and token tiles of a batch (one barrier
+// handshake per batch), one scale slot their scales, one TMEM buffer their
+// partials side by side.  A stage and a TMEM buffer hold XR token rows
+// (columns) in all.  A batch has GB groups of NT token rows; with VAR (the
+// masked layout, where the slot size NT is fixed but the expert's count is
+// known only on the device) gb = min(GB, XR / n) groups of n token rows, n
+// the count rounded up to 16.
 template <int NT, int STAGES, int SC, int GB, bool QX = false>
 struct SmallLayout {
+    static constexpr int XR = GB * NT < 256 ? GB * NT : 256;  // token rows per stage / TMEM columns per buffer
     static constexpr size_t w_group = (size_t)BM * BK;        // 16 KB of weights per K group
-    static constexpr size_t x_group = (size_t)NT * BK;        // tokens, E4M3 (swizzled, read by the MMA)
     static constexpr size_t xb_group = QX ? (size_t)NT * BK * 2 : 0;   // tokens as BF16 (quantized in the kernel)
     static constexpr size_t w_bytes = GB * w_group;           // per stage (batch)
-    static constexpr size_t x_bytes = GB * x_group;
+    static constexpr size_t x_bytes = (size_t)XR * BK;        // tokens, E4M3 (swizzled, read by the MMA)
     static constexpr size_t xb_bytes = GB * xb_group;
     static constexpr size_t off_w = 0;
     static constexpr size_t off_x = off_w + STAGES * w_bytes;
@@ -667,7 +671,8 @@ struct SmallLayout {
     static constexpr size_t off_sa = stage_end > part_bytes ? stage_end : part_bytes;
     static constexpr size_t off_sb = off_sa + (size_t)SC * sa_slot;
     static constexpr size_t off_bar = align_up(off_sb + (size_t)SC * sb_slot, 16);
-    static constexpr int bufcols = GB * NT;                    // TMEM columns of one batch's partials
+    static constexpr int bufcols = XR;                         // TMEM columns of one batch's partials
+    static_assert(!QX || GB * NT <= 256, "quantize-in-GEMM batches are whole");
     // as many TMEM buffers as fit (up to 8): the MMA runs that many batches ahead
     static constexpr int nbuf = (512 / bufcols) < 8 ? (512 / bufcols) : 8;
     static constexpr int num_bars = 2 * STAGES + 2 * SC + 2 * nbuf + 1 + (QX ? STAGES : SC);
@@ -682,7 +687,7 @@ struct SmallLayout {
 // kernel (no E4M3 round trip through HBM): warps 2 and 3 turn each K group's
 // BF16 token tile into the swizzled E4M3 tile the MMA reads and its scales,
 // by the same rule and code as the quantization kernels (e4m3_rule.cuh).
-template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX>
+template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_smallm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -731,7 +736,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t kb0 = (int32_t)((int64_t)split * p.KB / p.S);
     const int32_t kb1 = (int32_t)((int64_t)(split + 1) * p.KB / p.S);
     const int32_t ngroups = kb1 - kb0;
-    const int32_t nbatch = (ngroups + GB - 1) / GB;
+    // K groups per batch and the token rows (TMEM columns) of each group's tile
+    const int32_t ncol = VAR ? nt_run : NT;
+    const int32_t gb = VAR ? (L::XR / nt_run < GB ? L::XR / nt_run : GB) : GB;
+    const uint32_t xg = (uint32_t)ncol * BK;
+    const int32_t nbatch = (ngroups + gb - 1) / gb;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -758,28 +767,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one batch of weight and token tiles into stage b % STAGES
     auto issue_batch = [&](int32_t b) {
         const uint32_t s = b % STAGES;
-        const int32_t gn = min(GB, ngroups - b * GB);
+        const int32_t gn = min(gb, ngroups - b * gb);
         mbar_arrive_expect_tx(&full[s], (uint32_t)(gn * (L::w_group + nt_run * BK * (QX ? 2 : 1))));
         for (int32_t jj = 0; jj < gn; ++jj) {
-            const int32_t kx = (kb0 + b * GB + jj) * BK;
+            const int32_t kx = (kb0 + b * gb + jj) * BK;
             tma_load_2d(sm_w + s * L::w_bytes + jj * L::w_group, &tmW, &full[s], kx, (int32_t)(e * p.N) + tile * BM);
             for (int32_t r = 0; r < nt_run; r += 16) {   // 16-row boxes: whole 128B-swizzle atoms
                 if (QX)
                     tma_load_2d(sm_xb + s * L::xb_bytes + jj * L::xb_group + r * BK * 2, &tmX, &full[s], kx,
                                 (int32_t)(e * p.cap) + r);
                 else
-                    tma_load_2d(sm_x + s * L::x_bytes + jj * L::x_group + r * BK, &tmX, &full[s], kx,
+                    tma_load_2d(sm_x + s * L::x_bytes + jj * xg + r * BK, &tmX, &full[s], kx,
                                 (int32_t)(e * p.cap) + r);
             }
         }
     };
     // the scales of batch b: a (NT x GB) box of sa and a (4 x GB) box of the
-    // weight tile's block scales; boxes past the tensor read zeros
+    // weight tile's block scales from the batch's first K group (rows past
+    // the batch are not used; boxes past the tensor read zeros)
     auto issue_scales = [&](int32_t b) {
         const uint32_t j = b % SC;
         mbar_arrive_expect_tx(&sc_full[j], (uint32_t)(GB * NT * 4 + GB * 16));
-        tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + b * GB);
-        tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + b * GB);
+        tma_load_2d(sm_sa + j * L::sa_slot, &tmSA, &sc_full[j], (int32_t)(e * p.cap), kb0 + b * gb);
+        tma_load_2d(sm_sb + j * L::sb_slot, &tmSB, &sc_full[j], tile & ~3, e * p.KB + kb0 + b * gb);
     };
     // The first batch goes out before the block-wide barrier (the TMEM
     // allocation runs meanwhile): its stage and scale slot are unused, and
@@ -844,12 +854,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const int32_t gn = min(GB, ngroups - b * GB);
+            const int32_t gn = min(gb, ngroups - b * gb);
             float *sav = reinterpret_cast<float *>(sm_sa + j * L::sa_slot);
             for (int32_t jj = 0; jj < gn; ++jj) {
                 const uint8_t *xb = sm_xb + s * L::xb_bytes + jj * L::xb_group;
-                uint8_t *xq = sm_x + s * L::x_bytes + jj * L::x_group;
-                const float sbw = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + b * GB + jj) * p.ldsb + tile);
+                uint8_t *xq = sm_x + s * L::x_bytes + jj * xg;
+                const float sbw = __ldg(p.sb + (int64_t)(e * p.KB + kb0 + b * gb + jj) * p.ldsb + tile);
                 for (int32_t r0 = 0; r0 < nt_run; r0 += 4) {
                     const int r = r0 + 2 * wq + (int)(lane >> 4);
                     float f[8];
@@ -883,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
                 break;
             }
-            const int32_t gn = min(GB, ngroups - b * GB);
+            const int32_t gn = min(gb, ngroups - b * gb);
             float *sav = reinterpret_cast<float *>(sm_sa + j * L::sa_slot);
             const float *sbv = reinterpret_cast<const float *>(sm_sb + j * L::sb_slot);
             for (int32_t jj = 0; jj < gn; ++jj) {
@@ -924,13 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             if (elect_one()) {
-                const int32_t gn = min(GB, ngroups - b * GB);
+                const int32_t gn = min(gb, ngroups - b * gb);
                 for (int32_t jj = 0; jj < gn; ++jj) {
                     const uint64_t dw = smem_desc_kmajor_sw128(sm_w + s * L::w_bytes + jj * L::w_group);
-                    const uint64_t dx = smem_desc_kmajor_sw128(sm_x + s * L::x_bytes + jj * L::x_group);
+                    const uint64_t dx = smem_desc_kmajor_sw128(sm_x + s * L::x_bytes + jj * xg);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        mma_e4m3(tmem_base + buf * L::bufcols + jj * NT, dw + 2 * k, dx + 2 * k, idesc,
+                        mma_e4m3(tmem_base + buf * L::bufcols + jj * ncol, dw + 2 * k, dx + 2 * k, idesc,
                                  k > 0 ? 1u : 0u);
                 }
                 mma_commit(&empty[s]);
@@ -967,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int32_t gn = min(GB, ngroups - b * GB);
+            const int32_t gn = min(gb, ngroups - b * gb);
             // per token: sb(weight block) * sa(token), the same for every weight row
             const float *scl = reinterpret_cast<const float *>(sm_sa + j * L::sa_slot);
 #pragma unroll
@@ -977,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < COLS; c += CH) {
                     if ((int32_t)(col0 + c) >= nt_run) break;  // no token columns left (warp-uniform)
                     uint32_t r[CH];
-                    tmem_ld_sync<CH>(tmem_base + lane_addr + buf * L::bufcols + jj * NT + col0 + c, r);
+                    tmem_ld_sync<CH>(tmem_base + lane_addr + buf * L::bufcols + jj * ncol + col0 + c, r);
 #pragma unroll
                     for (int i = 0; i < CH / 4; ++i) {
                         const float4 s4 = *reinterpret_cast<const float4 *>(scl + jj * NT + col0 + c + 4 * i);
@@ -1443,7 +1453,7 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
                      : launch_variant<BN, STAGES, 8, 3, false, false>(a, p, grid, stream);
 }
 
-template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX = false>
+template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX = false, bool VAR = false>
 cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
     using L = SmallLayout<NT, STAGES, SC, GB, QX>;
@@ -1476,7 +1486,7 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
                !make_tensor_map_2d(&tmSB, 4, true, a.sb, a.ldsb, (uint64_t)E * p.KB, a.ldsb * 4, 4, GB, false)) {
         return cudaErrorInvalidValue;
     }
-    auto kern = gemm_smallm_kernel<NT, STAGES, SC, GB, OUT_F32, QX>;
+    auto kern = gemm_smallm_kernel<NT, STAGES, SC, GB, OUT_F32, QX, VAR>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
     // the S splits of a weight tile: one cluster of S consecutive CTAs
@@ -1498,7 +1508,7 @@ cudaError_t launch_small(const GemmArgs &a, cudaStream_t stream, int num_sms)
 template <bool OUT_F32>
 cudaError_t launch_small_nt(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
-    switch (small_nt(a.counts != nullptr ? a.cap : a.M)) {
+    switch (small_nt(a.M)) {
     // <tokens, stages, scale slots, K groups per batch>: batches of 4 K groups
     // (2 and 1 where four partials would not fit in tensor memory), stages
     // up to ~220 KB of shared memory
@@ -1591,9 +1601,27 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
     return launch_bn<256, 4>(a, stream, num_sms);
 }
 
+namespace {
+// Masked layout: the slot capacity fixes the layout, the expert's count (on
+// the device) the token rows computed.  Up to four K groups per batch, as
+// many as the 256 token rows of a stage and a TMEM buffer hold at the
+// expert's count (a full 256-row slot: one).
+template <bool OUT_F32>
+cudaError_t launch_masked_cap(const GemmArgs &a, cudaStream_t stream, int num_sms)
+{
+    switch (small_nt(a.cap)) {
+    case 16: return launch_small<16, 3, 3, 4, OUT_F32, false, true>(a, stream, num_sms);
+    case 32: return launch_small<32, 2, 4, 4, OUT_F32, false, true>(a, stream, num_sms);
+    case 64: return launch_small<64, 2, 4, 4, OUT_F32, false, true>(a, stream, num_sms);
+    case 128: return launch_small<128, 2, 4, 4, OUT_F32, false, true>(a, stream, num_sms);
+    default: return launch_small<256, 2, 4, 4, OUT_F32, false, true>(a, stream, num_sms);
+    }
+}
+}  // namespace
+
 cudaError_t launch_masked(const GemmArgs &a, cudaStream_t stream, int num_sms)
 {
-    return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
+    return a.out_f32 ? launch_masked_cap<true>(a, stream, num_sms) : launch_masked_cap<false>(a, stream, num_sms);
 }
 
 namespace {

@@ -534,9 +534,14 @@ def _run_masked(w, dt, rows=None, workspace=None):
 
 
 # E x weight tiles below the SM count -> K split over a cluster per (expert,
-# weight tile); 40 x 4 tiles -> one split, direct stores; token widths 16, 64, 256
+# weight tile); 40 x 4 tiles -> one split, direct stores; token widths 16, 64, 256.
+# A slot batches as many K groups as its expert's count allows: counts of 80,
+# 48, 112 in 256-row slots give 3, 4, 2 groups per batch at odd token offsets,
+# and 11 or 9 K groups leave ragged last batches.
 @pytest.mark.parametrize("counts,cap,N,K", [([64, 5, 0, 33], 64, 256, 512), ([16, 1], 16, 128, 256),
                                             ([256, 0, 200, 17, 1, 128, 255, 64], 256, 512, 1024),
+                                            ([80, 48, 112, 96, 176, 16], 256, 256, 1408),
+                                            ([128, 40, 72, 0, 100], 128, 384, 1152),
                                             ([int(c) for c in np.random.default_rng(5).integers(0, 33, 40)], 32, 512, 512)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
 def test_masked_grouped(counts, cap, N, K, out):
