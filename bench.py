@@ -44,6 +44,8 @@ FUSED_A_MAX_M = 256         # token count up to which fp8_gemm_bf16a_blockscaled
 # string, which changes whenever a kernel changes, so a stale figure is never
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
+    "fgf8 0.13 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md
+    },
     # 0.12 changed the masked-layout small-M launch only: the prefill GEMMs run the 0.10 kernel
     "fgf8 0.12 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md
         "prefill_pair_4096x18432x7168/up.gemm": 167797760 + 126922240,

@@ -47,6 +47,7 @@ EXPORTED = ["fgf8_status_string", "fgf8_version", "fp8_quant_act_1x128", "fp8_qu
             "fgf8_masked_gemm_workspace_bytes",
             "fgf8_read_status", "fgf8_mma_probe", "fgf8_selftest_wait_timeout", "fgf8_selftest_scaled_div",
             "fgf8_testing_gemm_schedule", "fgf8_testing_pair_clusters", "fgf8_testing_set_pair",
+            "fgf8_testing_multicast_clusters",
             "fgf8_testing_set_small_splits",
             "fgf8_noalloc_read_status"]
 
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.fgf8_testing_gemm_schedule.argtypes = [I64, I64, I64, I32, SZ, I32, P]
         L.fgf8_testing_pair_clusters.argtypes = []
         L.fgf8_testing_pair_clusters.restype = I32
+        L.fgf8_testing_multicast_clusters.argtypes = []
+        L.fgf8_testing_multicast_clusters.restype = I32
         L.fgf8_testing_set_pair.argtypes = [I32]
         L.fgf8_testing_set_pair.restype = ctypes.c_int
         L.fgf8_testing_set_small_splits.argtypes = [I32]

@@ -75,7 +75,7 @@ const char *fgf8_status_string(fgf8_status st)
 
 const char *fgf8_version(void)
 {
-    return "fgf8 0.12 sm_103a";
+    return "fgf8 0.13 sm_103a";
 }
 
 fgf8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
@@ -419,7 +419,7 @@ fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t 
 
 fgf8_status fgf8_testing_set_pair(int32_t mode)
 {
-    if (mode != 0 && mode != 1) return FGF8_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 2) return FGF8_ERR_INVALID_ARG;
     fgf8::set_pair_mode(mode);
     return FGF8_OK;
 }
@@ -435,6 +435,12 @@ int32_t fgf8_testing_pair_clusters(void)
 {
     if (current_device(nullptr) != FGF8_OK) return 0;
     return fgf8::pair_max_clusters();
+}
+
+int32_t fgf8_testing_multicast_clusters(void)
+{
+    if (current_device(nullptr) != FGF8_OK) return 0;
+    return fgf8::mc_max_clusters();
 }
 
 }  // extern "C"

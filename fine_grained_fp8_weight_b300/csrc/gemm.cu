@@ -80,7 +80,8 @@ enum : int32_t {
 struct Params {
     int64_t M, N, K;
     int32_t KB;
-    int32_t num_m_blocks, num_n_blocks, num_tiles;
+    int32_t num_m_blocks, num_n_blocks, num_tiles;   // with multicast clusters: rows of MC M blocks
+    int32_t m_blocks;                   // 128-row blocks of A
     int32_t m_major;                    // tile order: 1 = m outer, 0 = n outer within bands of M blocks
     int32_t band;                       // n outer: M blocks per band (all of them when A fits in L2)
     void *C;
@@ -92,7 +93,8 @@ struct Params {
     const float *sa;                    // scales, copied by the scale warp with cp.async
     const float *sb;
     int64_t ldsa, ldsb;
-    // Tail split: tiles [0, dp_tiles) run whole, tile t on CTA t mod G; the
+    // Tail split (with multicast: cluster tiles on clusters):
+    // tiles [0, dp_tiles) run whole, tile t on CTA t mod G; the
     // other R = num_tiles - dp_tiles tiles (fewer than G) are each cut into
     // tail_s contiguous K-group pieces, unit v = piece * R + tail tile on CTA v,
     // so the last wave keeps every SM busy.  The last piece of a tail tile to
@@ -104,10 +106,13 @@ struct Params {
 };
 
 // The segments (tile, K groups k0..k1, tail piece or -1) one CTA processes, in
-// order; every role of the CTA walks the same sequence.
+// order; every role of the CTA walks the same sequence.  With clusters of MC
+// CTAs (multicast) both CTAs of a cluster walk the same cluster tiles: the
+// walk goes by cluster index and cluster count.
+template <int MC>
 struct SegIter {
     int32_t t, v;
-    __device__ __forceinline__ SegIter() : t((int32_t)blockIdx.x), v((int32_t)blockIdx.x) {}
+    __device__ __forceinline__ SegIter() : t((int32_t)(blockIdx.x / MC)), v((int32_t)(blockIdx.x / MC)) {}
     __device__ __forceinline__ bool next(const Params &p, int32_t &tile, int32_t &k0, int32_t &k1, int32_t &piece)
     {
         if (t < p.dp_tiles) {
@@ -115,7 +120,7 @@ struct SegIter {
             k0 = 0;
             k1 = p.KB;
             piece = -1;
-            t += gridDim.x;
+            t += gridDim.x / MC;
             return true;
         }
         if (v >= p.tail_units) return false;
@@ -124,7 +129,7 @@ struct SegIter {
         tile = p.dp_tiles + (v - piece * R);
         k0 = piece * p.KB / p.tail_s;
         k1 = (piece + 1) * p.KB / p.tail_s;
-        v += gridDim.x;
+        v += gridDim.x / MC;
         return true;
     }
 };
@@ -197,7 +202,12 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, float2 a, float
     *reinterpret_cast<uint4 *>(dst) = o;
 }
 
-template <int BN, int STAGES, int SG, int SS, bool ROW_SB, bool OUT_F32>
+// MC = 2: the kernel runs in clusters of two CTAs on vertically adjacent
+// tiles (M blocks 2r and 2r + 1, the same N block).  Each CTA loads its own
+// A panel and one half of the shared B panel, multicast into both CTAs'
+// stages; a stage is refilled once both CTAs' MMAs have read it (each MMA
+// warp's commit arrives on the stage's barrier in both CTAs).
+template <int BN, int STAGES, int SG, int SS, bool ROW_SB, bool OUT_F32, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const Params p)
@@ -223,11 +233,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
+    static_assert(MC == 1 || MC == 2, "clusters of one or two CTAs");
+    const uint32_t crank = MC > 1 ? cluster_ctarank() : 0;
+    // this CTA's M block and the N block of a (cluster) tile
+    auto tile_mb = [&](int32_t tile, int32_t &mb, int32_t &nb) {
+        tile_coords(tile, p, mb, nb);
+        mb = mb * MC + (int32_t)crank;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], MC);                   // every CTA's MMA warp frees the stage
         }
         for (int i = 0; i < SS; ++i) {
             mbar_init(&sc_full[i], 32);                 // one cp.async arrival per scale-warp lane
@@ -244,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) tmem_alloc(tmem_base_slot, L::tmem_cols);
     tc_fence_before_sync();
     __syncthreads();
+    if (MC > 1) cluster_sync();                         // the peer may now fill this CTA's stages
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_slot;
 
@@ -255,14 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmB);
             uint32_t it = 0;
             bool ok = true;
-            SegIter si;
+            SegIter<MC> si;
             int32_t tile, kbeg, kend, piece;
             while (ok && si.next(p, tile, kbeg, kend, piece)) {
                 int32_t mb, nb;
-                tile_coords(tile, p, mb, nb);
+                tile_mb(tile, mb, nb);
                 const int32_t e = block_expert(p, mb);
                 if (e < 0) continue;
                 const int32_t b_row = (int32_t)(e * p.b_rows_per_expert) + nb * BN;
+                // an M block past the end (odd block count, second CTA of the
+                // last cluster row) loads the last block; its rows are not stored
+                const int32_t a_row = (MC == 1 || mb < p.m_blocks ? mb : p.m_blocks - 1) * BM;
                 for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
@@ -271,8 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(L::a_bytes + L::b_bytes));
-                    tma_load_2d(sm_a + s * L::a_bytes, &tmA, &full[s], kb * BK, mb * BM);
-                    tma_load_2d(sm_b + s * L::b_bytes, &tmB, &full[s], kb * BK, b_row);
+                    tma_load_2d(sm_a + s * L::a_bytes, &tmA, &full[s], kb * BK, a_row);
+                    if (MC > 1)
+                        tma_load_2d_multicast(sm_b + s * L::b_bytes + crank * (L::b_bytes / MC), &tmB, &full[s],
+                                              kb * BK, b_row + (int32_t)crank * (BN / MC), (uint16_t)((1u << MC) - 1));
+                    else
+                        tma_load_2d(sm_b + s * L::b_bytes, &tmB, &full[s], kb * BK, b_row);
                 }
             }
             if (!ok) {
@@ -293,11 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Every segment (tile or tail piece) starts a new slot.
         uint32_t nslot = 0;
         bool ok = true;
-        SegIter si;
+        SegIter<MC> si;
         int32_t tile, kbeg, kend, piece;
         while (ok && si.next(p, tile, kbeg, kend, piece)) {
             int32_t mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_mb(tile, mb, nb);
             const int32_t e = block_expert(p, mb);
             if (e < 0) continue;
             const int64_t s_row0 = (int64_t)e * p.sb_rows_per_expert;
@@ -336,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc = idesc_e4m3_f32(BM, BN);
         uint32_t it = 0;
         bool ok = true;
-        SegIter si;
+        SegIter<MC> si;
         int32_t tile, kbeg, kend, piece;
         while (ok && si.next(p, tile, kbeg, kend, piece)) {
             int32_t mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_mb(tile, mb, nb);
             if (block_expert(p, mb) < 0) continue;
             for (int32_t kb = kbeg; kb < kend; ++kb, ++it) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
@@ -366,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)       // 32 bytes = 2 x 16-byte descriptor units
                         mma_e4m3(d_tmem, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
-                    mma_commit(&empty[s]);
+                    if (MC > 1)
+                        mma_commit_multicast(&empty[s], (uint16_t)((1u << MC) - 1));
+                    else
+                        mma_commit(&empty[s]);
                     mma_commit(&tm_full[buf]);
                 }
                 __syncwarp();
@@ -400,11 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         // After a failed wait a warp still walks its remaining segments (without
         // waiting), so that all eight reach the tail's named barrier together.
-        SegIter si;
+        SegIter<MC> si;
         int32_t tile, kbeg, kend, piece;
         while (si.next(p, tile, kbeg, kend, piece)) {
             int32_t mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_mb(tile, mb, nb);
             if (block_expert(p, mb) < 0) continue;
             float2 acc[HALF / 2];
 #pragma unroll
@@ -482,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (piece >= 0) {
                 // A piece of a tail tile: store the FP32 partial, take a ticket;
-                // the last piece to arrive adds all of them in K order.
-                const int32_t ti = tile - p.dp_tiles;
+                // the last piece to arrive adds all of them in K order.  (With
+                // multicast clusters each CTA of a tail cluster tile owns one.)
+                const int32_t ti = (tile - p.dp_tiles) * MC + (int32_t)crank;
                 if (ok) {
                     float *mine = p.tail_partials + (int64_t)(ti * p.tail_s + piece) * (BM * BN);
                     if constexpr (ROW_SB) {
@@ -601,6 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    // no multicast copy or commit arrival of the peer is left in flight
+    if (MC > 1) cluster_sync();
     if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, L::tmem_cols);
@@ -1247,23 +1278,77 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int BN, int STAGES, int SG, int SS, bool ROW_SB, bool OUT_F32>
+template <int BN, int STAGES, int SG, int SS, bool ROW_SB, bool OUT_F32, int MC = 1>
 cudaError_t launch_variant(const GemmArgs &a, const Params &p, int grid, cudaStream_t stream)
 {
     using L = Layout<BN, STAGES, SG, SS, ROW_SB>;
     CUtensorMap tmA, tmB;
     const int64_t b_rows = a.m_indices ? (int64_t)a.num_experts * a.N : a.N;
+    // with multicast each CTA of a cluster loads one of MC row slices of the B panel
     if (!make_tensor_map_2d(&tmA, 1, false, a.A, a.K, a.M, a.K, BK, BM, true) ||
-        !make_tensor_map_2d(&tmB, 1, false, a.B, a.K, b_rows, a.K, BK, BN, true))
+        !make_tensor_map_2d(&tmB, 1, false, a.B, a.K, b_rows, a.K, BK, BN / MC, true))
         return cudaErrorInvalidValue;
-    auto kern = gemm_blockscaled_kernel<BN, STAGES, SG, SS, ROW_SB, OUT_F32>;
+    auto kern = gemm_blockscaled_kernel<BN, STAGES, SG, SS, ROW_SB, OUT_F32, MC>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, L::dyn_bytes, stream>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    if (MC == 1) {
+        kern<<<grid, kThreads, L::dyn_bytes, stream>>>(tmA, tmB, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::dyn_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = MC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
+int g_mc_clusters[64];          // concurrent clusters of the multicast variant per device (0: not yet known)
+
 }  // namespace
+
+// Concurrent clusters of two of the multicast variant on the current device
+// (looked up once per device; 0 if it cannot run).
+int mc_max_clusters()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (g_mc_clusters[dev] == 0) {
+        using L = Layout<256, 4, 8, 3, false>;
+        auto kern = gemm_blockscaled_kernel<256, 4, 8, 3, false, false, 2>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = L::dyn_bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            g_mc_clusters[dev] = -1;
+        } else {
+            g_mc_clusters[dev] = n;
+        }
+    }
+    return g_mc_clusters[dev] > 0 ? g_mc_clusters[dev] : 0;
+}
 
 bool make_tensor_map_2d(void *map, int dtype_bytes, bool is_float, const void *base, uint64_t inner, uint64_t outer,
                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128)
@@ -1393,7 +1478,7 @@ namespace {
 // for the B panels and output passing through).
 constexpr int64_t kBandBytes = 48ll << 20;
 
-template <int BN>
+template <int BN, int MC = 1>
 Params make_params(const GemmArgs &a)
 {
     Params p{};
@@ -1401,7 +1486,8 @@ Params make_params(const GemmArgs &a)
     p.N = a.N;
     p.K = a.K;
     p.KB = (int32_t)(a.K / BK);
-    p.num_m_blocks = (int32_t)((a.M + BM - 1) / BM);
+    p.m_blocks = (int32_t)((a.M + BM - 1) / BM);
+    p.num_m_blocks = (p.m_blocks + MC - 1) / MC;
     p.num_n_blocks = (int32_t)((a.N + BN - 1) / BN);
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.m_major = a.m_indices != nullptr ? 1 : 0;
@@ -1409,7 +1495,7 @@ Params make_params(const GemmArgs &a)
     // possible: the down projection 4096 x 7168 x 18432 (A 75.5 MB) walks two
     // bands, reading A once and B twice instead of A once per wave.
     {
-        const int64_t a_bytes = (int64_t)p.num_m_blocks * BM * a.K;
+        const int64_t a_bytes = (int64_t)p.m_blocks * BM * a.K;
         const int64_t nbands = (a_bytes + kBandBytes - 1) / kBandBytes;
         p.band = (int32_t)((p.num_m_blocks + nbands - 1) / nbands);
     }
@@ -1451,6 +1537,32 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t stream, int num_sms)
                          : launch_variant<BN, STAGES, 4, 3, true, false>(a, p, grid, stream);
     return a.out_f32 ? launch_variant<BN, STAGES, 8, 3, false, true>(a, p, grid, stream)
                      : launch_variant<BN, STAGES, 8, 3, false, false>(a, p, grid, stream);
+}
+
+// Clusters of two vertically adjacent 128 x 256 tiles sharing the B panel by
+// TMA multicast (dense GEMMs, 128x128 block B scales), the last wave split
+// along K over clusters as launch_bn does over CTAs.
+cudaError_t launch_multicast(const GemmArgs &a, cudaStream_t stream)
+{
+    Params p = make_params<256, 2>(a);
+    const int G = mc_max_clusters();
+    if (G <= 0) return cudaErrorNotSupported;
+    int clusters = p.num_tiles < G ? p.num_tiles : G;
+    if (clusters <= 0) return cudaSuccess;
+    const TailPlan t = plan_tail(a, p.num_tiles, p.KB, G, a.ws_bytes >= tail_workspace_bytes(256));
+    p.dp_tiles = t.dp_tiles;
+    if (t.s > 1) {
+        const int32_t units = (p.num_tiles - t.dp_tiles) * t.s;
+        clusters = t.dp_tiles > 0 ? G : units;
+        p.tail_s = t.s;
+        p.tail_units = units;
+        uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+        p.tail_tickets = reinterpret_cast<uint32_t *>(ws + kWsHeaderBytes);
+        p.tail_partials = reinterpret_cast<float *>(ws + kWsPartialsOffset);
+    }
+    const int grid = 2 * clusters;
+    return a.out_f32 ? launch_variant<256, 4, 8, 3, false, true, 2>(a, p, grid, stream)
+                     : launch_variant<256, 4, 8, 3, false, false, 2>(a, p, grid, stream);
 }
 
 template <int NT, int STAGES, int SC, int GB, bool OUT_F32, bool QX = false, bool VAR = false>
@@ -1543,7 +1655,14 @@ int g_pair_mode = 0;
 
 bool use_pair(const GemmArgs &a)
 {
-    return g_pair_mode != 0 && a.m_indices == nullptr && a.counts == nullptr && a.bkind == 0 && a.M > BM;
+    return g_pair_mode == 1 && a.m_indices == nullptr && a.counts == nullptr && a.bkind == 0 && a.M > BM;
+}
+
+// Mode 2: dense block-scaled GEMMs of more than 128 rows run the 128 x 256
+// kernel in clusters of two that share B by TMA multicast.
+bool use_multicast(const GemmArgs &a)
+{
+    return g_pair_mode == 2 && a.m_indices == nullptr && a.counts == nullptr && a.bkind == 0 && a.M > BM;
 }
 
 void set_pair_mode(int mode)
@@ -1572,6 +1691,15 @@ GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
         g.tail_s = pl.tail_s;
         return g;
     }
+    if (use_multicast(a)) {
+        const int64_t tiles = ((a.M + 2 * BM - 1) / (2 * BM)) * ((a.N + 255) / 256);
+        const TailPlan t = plan_tail(a, tiles, a.K / BK, num_sms / 2, a.ws_bytes >= tail_workspace_bytes(256));
+        g.pair = 2;
+        g.bn = 256;
+        g.dp_tiles = t.dp_tiles;
+        g.tail_s = t.s;
+        return g;
+    }
     g.bn = choose_bn(a, num_sms);
     const int G = num_sms < kNominalSms ? num_sms : kNominalSms;
     const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + g.bn - 1) / g.bn);
@@ -1584,7 +1712,7 @@ GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms)
 size_t gemm_required_bytes(const GemmArgs &a, int num_sms)
 {
     const GemmSchedule g = gemm_schedule(a, num_sms);
-    if (g.tail_s > 1) return g.pair ? pair_tail_workspace_bytes() : tail_workspace_bytes(g.bn);
+    if (g.tail_s > 1) return g.pair == 1 ? pair_tail_workspace_bytes() : tail_workspace_bytes(g.bn);
     return kWsHeaderBytes;
 }
 
@@ -1595,6 +1723,10 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t stream, int num_sms)
         return a.out_f32 ? launch_small_nt<true>(a, stream, num_sms) : launch_small_nt<false>(a, stream, num_sms);
     if (use_pair(a)) {
         const cudaError_t e = launch_pair(a, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    if (use_multicast(a)) {
+        const cudaError_t e = launch_multicast(a, stream);
         if (e != cudaErrorNotSupported) return e;
     }
     if (choose_bn(a, num_sms) == 128) return launch_bn<128, 6>(a, stream, num_sms);

@@ -71,9 +71,12 @@ struct GemmSchedule {
     int small_m, bn, dp_tiles, tail_s, pair;
 };
 GemmSchedule gemm_schedule(const GemmArgs &a, int num_sms);
-// 1: dense block-scaled GEMMs of more than 128 rows run on CTA pairs; 0: the
-// planner's choice (single-SM tiles).  Process-wide, for tests.
+// 1: dense block-scaled GEMMs of more than 128 rows run on CTA pairs; 2: they
+// run single-SM tiles in clusters of two sharing B by TMA multicast; 0: the planner's choice (single-SM tiles).
+// Process-wide, for tests.
 void set_pair_mode(int mode);
+// Concurrent two-CTA clusters of the multicast variant on the current device.
+int mc_max_clusters();
 // 1..8: the dense small-M kernel splits K over this many CTAs (at most K/128);
 // 0: the planner's choice.  Process-wide, for tests.
 void set_small_splits(int s);

@@ -149,6 +149,20 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// The same load, multicast: the box lands at smem_dst's offset in every CTA
+// of this cluster named in cta_mask, and each of them counts the bytes it
+// received on its own mbarrier at bar's offset.  The tensor map covers this
+// GPU's memory only.
+__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                                      int32_t x, int32_t y, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+        "{%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
+        : "memory");
+}
+
 // ------------------------------------------------------ tensor memory --
 
 // Allocate `ncols` (power of two >= 32) TMEM columns; the base address is
@@ -328,6 +342,18 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_addr(bar))
                  : "memory");
+}
+
+// Arrive once on the mbarrier at bar's offset in each CTA of this cluster
+// named in cta_mask when every tcgen05.mma issued so far by this thread has
+// completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // ------------------------------------------------ CTA pairs (clusters) --

@@ -45,12 +45,15 @@ fgf8_status fgf8_selftest_scaled_div(const float *x, const float *s, int64_t n, 
  *   schedule[1] = output tile width (128 or 256 columns);
  *   schedule[2] = tiles computed whole (a multiple of the number of
  *                 concurrent CTAs, or CTA pairs, when the last wave is
- *                 split, else all of them);
+ *                 split, else all of them); with multicast clusters a tile
+ *                 is a cluster tile of two 128-row blocks;
  *   schedule[3] = K pieces per remaining tile (1 = no split); for the
  *                 small-M kernel, the CTAs (one cluster) that split the K
  *                 groups of each 128-row weight tile;
  *   schedule[4] = 1 if the CTA-pair kernel runs (256 x 128 tiles on two SMs;
- *                 num_sms / 2 pairs are assumed), 0 for 128-row tiles.
+ *                 num_sms / 2 pairs are assumed), 2 if 128 x 256 tiles run
+ *                 in clusters of two sharing B by TMA multicast (num_sms / 2
+ *                 clusters assumed), 0 for 128-row tiles on single CTAs.
  * `schedule` points to 5 host int32.  Lets tests check the schedule choice on
  * a CPU and confirm that a GPU case covers the path it is meant to.
  */
@@ -63,6 +66,11 @@ fgf8_status fgf8_testing_gemm_schedule(int64_t M, int64_t N, int64_t K, int32_t 
  * small-M kernel takes) run on the CTA-pair kernel: 256 x 128 output tiles on
  * two SMs whose tensor cores work as one (tcgen05 .cta_group::2), four FP32
  * partial buffers per SM, even and odd K groups promoted by different warps.
+ * 2: dense GEMMs with 128x128 block scales and more than 128 rows run the
+ * 128 x 256 single-SM kernel in clusters of two CTAs on vertically adjacent
+ * tiles: each CTA loads its own A panel and half of the B panel they share,
+ * multicast into both (cp.async.bulk.tensor .multicast::cluster, this GPU's
+ * memory only), and each MMA warp's commit frees the stage in both CTAs.
  * 0: back to the planner's choice (128-row tiles on single SMs, which are
  * faster on the B300).  Returns FGF8_ERR_INVALID_ARG for other values.  Not
  * thread-safe: set it while no other thread calls the library.
@@ -87,6 +95,15 @@ fgf8_status fgf8_testing_set_small_splits(int32_t splits);
  * the device actually runs.
  */
 int32_t fgf8_testing_pair_clusters(void);
+
+/*
+ * fgf8_testing_multicast_clusters -- the number of two-CTA clusters of the
+ * multicast variant (fgf8_testing_set_pair(2)) that the current device runs
+ * at once (0 if it cannot run it); an occupancy query, launches nothing.
+ * Twice this number as `num_sms` gives fgf8_testing_gemm_schedule the
+ * schedule the device runs in that mode.
+ */
+int32_t fgf8_testing_multicast_clusters(void);
 
 #ifdef __cplusplus
 }

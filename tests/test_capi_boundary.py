@@ -280,8 +280,38 @@ def test_pair_schedule_of_the_prefill_pair(L, pair_on):
 
 
 def test_set_pair_rejects(L):
-    assert L.fgf8_testing_set_pair(2) == 1
+    assert L.fgf8_testing_set_pair(3) == 1
     assert L.fgf8_testing_set_pair(-1) == 1
+
+
+@pytest.fixture
+def multicast_on(L):
+    """Clusters of two 128 x 256 tiles sharing B by TMA multicast, for one test."""
+    assert L.fgf8_testing_set_pair(2) == 0
+    try:
+        yield
+    finally:
+        assert L.fgf8_testing_set_pair(0) == 0
+
+
+@pytest.mark.parametrize("sms", [148, 132])
+def test_multicast_last_wave_split_invariants(L, multicast_on, sms):
+    """The same for multicast clusters: SMs / 2 clusters, cluster tiles of
+    two 128-row blocks x 256 columns."""
+    _check_split_invariants(sms, 0, 2)
+    assert fg.fgf8_testing_gemm_schedule(4096, 18432, 7168, 1)["pair"] == 0   # per-row B scales: single CTAs
+
+
+def test_multicast_schedule_of_the_prefill_pair(L, multicast_on):
+    # 4096 x 18432 x 7168 on 74 clusters: 16 x 72 = 1152 cluster tiles = 15
+    # waves + 42, run whole as on single CTAs (no split beats them);
+    # 4096 x 7168 x 18432: 448 = 6 waves + 4, cut into 8 K pieces each
+    assert fg.fgf8_testing_gemm_schedule(4096, 18432, 7168) == {"small_m": 0, "bn": 256, "dp_tiles": 1152,
+                                                                "tail_s": 1, "pair": 2}
+    assert fg.fgf8_testing_gemm_schedule(4096, 7168, 18432) == {"small_m": 0, "bn": 256, "dp_tiles": 444,
+                                                                "tail_s": 8, "pair": 2}
+    assert fg.fgf8_testing_gemm_schedule(128, 18432, 7168)["pair"] == 0   # one 128-row block
+    assert fg.fgf8_testing_gemm_schedule(64, 4096, 7168)["small_m"] == 1
 
 
 def test_schedule_rejects(L):

@@ -444,6 +444,117 @@ def _repeat_check(M, N, K, bkind, out):
         assert not bool(bad.any()), f"launch {i} differs at {bad.nonzero()[:4].tolist()}"
 
 
+# Multicast clusters (off by default, switched on by the test hook): two CTAs
+# on vertically adjacent 128 x 256 tiles, each loading its own A panel and half
+# of the B panel they share, multicast into both.  Odd 128-row block counts
+# leave the last cluster's second CTA past M (M = 384, 640, 129, 300, 1408,
+# 3200); N narrower than the shared half (48) or ending inside either half.
+@pytest.fixture
+def multicast_on():
+    assert fg.lib().fgf8_testing_set_pair(2) == 0
+    try:
+        yield
+    finally:
+        assert fg.lib().fgf8_testing_set_pair(0) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 256, 128), (384, 272, 512), (129, 18432, 256), (640, 48, 384),
+                                   (1000, 1040, 1152), (2048, 4096, 2048)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_multicast_shapes(M, N, K, out, multicast_on):
+    assert fg.fgf8_testing_gemm_schedule(M, N, K)["pair"] == 2
+    rng = np.random.default_rng(M * 5 + N * 3 + K)
+    A = wl.bf16_normal(rng, (M, K), 1.0, 0.01, 100.0)
+    B = wl.bf16_normal(rng, (N, K), 0.02)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    rows = _rows_per_block(M, 4, M + 1) if M * N * K > 2 ** 31 else None
+    Cg, Cr, S = _run_dense(A, B, dt, rows=rows)
+    assert_within_bound(Cg, Cr, S, f"multicast {M}x{N}x{K}")
+
+
+# Whole tiles (the least workspace: no K split) on multicast clusters compute
+# every element with the same MMAs and promotion as single CTAs with 256-column
+# tiles: equal bit for bit.
+@pytest.mark.parametrize("M,N,K", [(1408, 2304, 1024), (3200, 1024, 1024), (4096, 4096, 1024), (2048, 4096, 2048)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_multicast_whole_tiles_equal_single_cta(M, N, K, out):
+    g = torch.Generator(device="cpu").manual_seed(M + 3 * N + K)
+    qa = torch.randint(0, 256, (M, K), dtype=torch.uint8, generator=g)
+    qa[(qa & 0x7F) == 0x7F] = 0x3C                  # no NaN codes
+    qb = torch.randint(0, 256, (N, K), dtype=torch.uint8, generator=g)
+    qb[(qb & 0x7F) == 0x7F] = 0x3C
+    sa = torch.rand((K // 128, M), generator=g) + 0.5
+    sb = torch.rand((K // 128, ((N + 127) // 128 + 3) // 4 * 4), generator=g) + 0.5
+    args = [t.to(DEV) for t in (qa, sa, qb, sb)]
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    ws = torch.zeros(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), dtype=torch.uint8, device=DEV)
+    single = fg.fgf8_testing_gemm_schedule(M, N, K, ws_bytes=ws.numel())
+    assert single["bn"] == 256 and single["tail_s"] == 1 and single["pair"] == 0, single
+    ref = fg.fp8_gemm_blockscaled(*args, out_dtype=dt, workspace=ws, check=True)
+    assert fg.lib().fgf8_testing_set_pair(2) == 0
+    try:
+        assert fg.fgf8_testing_gemm_schedule(M, N, K, ws_bytes=ws.numel())["pair"] == 2
+        mc = fg.fp8_gemm_blockscaled(*args, out_dtype=dt, workspace=ws, check=True)
+        torch.cuda.synchronize()
+    finally:
+        assert fg.lib().fgf8_testing_set_pair(0) == 0
+    iv = torch.int16 if dt == torch.bfloat16 else torch.int32
+    bad = mc.view(iv) != ref.view(iv)
+    assert not bool(bad.any()), f"multicast differs from single CTAs at {bad.nonzero()[:4].tolist()}"
+
+
+@pytest.mark.parametrize("M,N,K", [(1280, 4096, 2048), (2560, 4096, 4096), (512, 2048, 2048), (3072, 1792, 2048)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_multicast_last_wave_split(M, N, K, out, multicast_on):
+    # the planner with the clusters this device runs at once: some cluster
+    # tiles are cut into K pieces; with the least workspace, whole tiles
+    sm = 2 * fg.lib().fgf8_testing_multicast_clusters()
+    sch = fg.fgf8_testing_gemm_schedule(M, N, K, 0, num_sms=sm)
+    assert sch["pair"] == 2 and sch["tail_s"] > 1, sch
+    ops, rows, Cr, S = _split_case(M, N, K, 0)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    ws_min = torch.zeros(fg.lib().fgf8_gemm_workspace_min_bytes(M, N, K, 1), dtype=torch.uint8, device=DEV)
+    for label, ws in (("split", None), ("whole tiles", ws_min)):
+        C = fg.fp8_gemm_blockscaled(*ops, out_dtype=dt, workspace=ws, check=True)
+        torch.cuda.synchronize()
+        Cg = bf16_out_to_f64(C) if dt == torch.bfloat16 else C.cpu().numpy().astype(np.float64)
+        assert_within_bound(Cg[rows], Cr, S, f"multicast {label} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,out", [(2048, 4096, 4096, "bf16"), (1280, 4096, 2048, "fp32"),
+                                       (3072, 1792, 2048, "bf16")])
+def test_multicast_repeated_launches_bitwise_identical(M, N, K, out, multicast_on):
+    _repeat_check(M, N, K, 0, out)
+
+
+def test_multicast_output_row_stride_and_untouched_padding(multicast_on):
+    # rows past M and columns past N of a larger output buffer stay as they
+    # were; 3 row blocks: the second CTA of the last cluster is past M
+    rng = np.random.default_rng(17)
+    A = wl.bf16_normal(rng, (300, 256))
+    B = wl.bf16_normal(rng, (272, 256), 0.02)
+    qa, sa = oracle.quant_act_1x128(A)
+    qb, sb = oracle.quant_w_128x128(B)
+    big = torch.full((512, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = big[:300, :272]
+    assert fg.fgf8_testing_gemm_schedule(300, 272, 256)["pair"] == 2
+    fg.fp8_gemm_blockscaled(_d(qa), _d(sa), _d(qb), _d(sb), out=out, check=True)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:, 272:]).all() and torch.isnan(big[300:]).all(), "elements past M or N were written"
+    Cr, S = oracle.gemm_blockscaled(qa, sa, qb, sb)
+    assert_within_bound(bf16_out_to_f64(out), Cr, S)
+
+
+def test_full_size_prefill_multicast_sampled(multicast_on):
+    # one row of every 128-row block: both CTAs of every cluster row
+    for g, seed in zip(wl.prefill_pair().gemms, (21, 22)):
+        (M, K), N = g.A.shape, g.B.shape[0]
+        assert fg.fgf8_testing_gemm_schedule(M, N, K)["pair"] == 2
+        rows = _rows_per_block(M, 1, seed)
+        Cg, Cr, S = _run_dense(g.A, g.B, torch.bfloat16, rows=rows)
+        report_margin(f"C2 {g.name} multicast (sampled rows)", assert_within_bound(Cg, Cr, S, g.name), Cg.size)
+
+
 # The grouped layout repeated: m-outer tile walk with several tiles per CTA,
 # expert changes inside a CTA's walk, padding blocks between experts and an
 # empty expert; the whole output (padding rows left NaN) must match bit for bit.
