@@ -45,6 +45,8 @@ FUSED_A_MAX_M = 256         # token count up to which fp8_gemm_bf16a_blockscaled
 # reported: a kernel without a capture of its current build reports null.
 MEASURED_TRAFFIC = {
     "fgf8 0.13 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md
+        "prefill_pair_4096x18432x7168/up.gemm": 166400000 + 126772480,
+        "prefill_pair_4096x18432x7168/down.gemm": 520134400 + 51309312,
     },
     # 0.12 changed the masked-layout small-M launch only: the prefill GEMMs run the 0.10 kernel
     "fgf8 0.12 sm_103a": {                                   # profiles/gemm_blockscaled_prefill_traffic.md
@@ -472,6 +474,12 @@ def run_device(args, rank, world, local_rank):
         step_graph.replay()
     barrier()
 
+    # Each kernel timed alone (its own graph, L2 flushed between replays)
+    # before the long step loop, which on a 1.1 kW part can run into the
+    # power cap and lower the clocks that follow it.
+    per_op = time_ops(path, dev, stream, max(3, min(args.op_reps, args.steps)), fp8_peak, peaks)
+    barrier()
+
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
@@ -486,7 +494,6 @@ def run_device(args, rank, world, local_rank):
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     ms_step = ms_total / args.steps
 
-    per_op = time_ops(path, dev, stream, max(3, min(args.op_reps, args.steps)), fp8_peak, peaks)
     n_ops = len(path.ops)
     value = job_tflops(path.gemm_flops, world, ms_step)
     version = fg.lib().fgf8_version().decode()
