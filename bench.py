@@ -536,15 +536,32 @@ def run_device(args, rank, world, local_rank):
     return result
 
 
+class L2Flush:
+    """Untimed L2 flush between replays: a write of a buffer twice the 126 MB
+    L2, so that no op finds inputs left in L2 by its previous replay, then a
+    read of a second such buffer, so that the L2 holds clean lines and the
+    timed op does not pay for writing the first buffer's dirty lines back to
+    HBM (2 us of a 20 us quantization otherwise)."""
+
+    def __init__(self, torch, dev):
+        n = 2 * 126 * 2 ** 20 // 4 + 2 ** 20
+        self.dirty = torch.empty(n, dtype=torch.float32, device=dev)
+        self.clean = torch.ones(n, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.dirty.fill_(1.0)
+        self.clean.sum()
+
+
 def time_ops(path, dev, stream, reps, fp8_peak, peaks):
     """Per-kernel device time: each op captured alone into a CUDA graph and
-    replayed, one event pair per replay (the median is reported), with an untimed write of a buffer
-    larger than L2 in between so that no op reads inputs left in L2 by its
-    previous replay.  A short device-side sleep before the first event keeps
-    the GPU busy while the host submits the event and the replay, so the
-    interval holds the op alone and not the host's submission latency."""
+    replayed, one event pair per replay (the median is reported), with an
+    untimed L2 flush (L2Flush) in between.  A short device-side sleep before
+    the first event keeps the GPU busy while the host submits the event and
+    the replay, so the interval holds the op alone and not the host's
+    submission latency."""
     import torch
-    flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     per_op = {}
     for kind, name, fn, work_units in path.ops:
         g = torch.cuda.CUDAGraph()
@@ -557,7 +574,7 @@ def time_ops(path, dev, stream, reps, fp8_peak, peaks):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         g.replay()
         for e0, e1 in ev:
-            flush.fill_(1.0)
+            flush()
             torch.cuda._sleep(SLEEP_CYCLES)
             e0.record()
             g.replay()
@@ -585,7 +602,7 @@ def time_ops_rotating(paths, dev, stream, reps, fp8_peak, peaks):
     inputs in L2 and the start of a replay is spread over many kernels; the L2
     is flushed before each timed replay.  Reports the mean time per launch."""
     import torch
-    flush = torch.empty(2 * 126 * 2 ** 20 // 4 + 2 ** 20, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     R = len(paths)
     per_op = {}
     for j, (kind, name, _, work_units) in enumerate(paths[0].ops):
@@ -602,7 +619,7 @@ def time_ops_rotating(paths, dev, stream, reps, fp8_peak, peaks):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         g.replay()
         for e0, e1 in ev:
-            flush.fill_(1.0)
+            flush()
             torch.cuda._sleep(SLEEP_CYCLES)
             e0.record()
             g.replay()
