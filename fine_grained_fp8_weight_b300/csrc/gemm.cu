@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -1310,7 +1311,7 @@ cudaError_t launch_variant(const GemmArgs &a, const Params &p, int grid, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
-int g_mc_clusters[64];          // concurrent clusters of the multicast variant per device (0: not yet known)
+std::atomic<int> g_mc_clusters[64];          // concurrent clusters of the multicast variant per device (0: not yet known)
 
 }  // namespace
 
@@ -1320,7 +1321,7 @@ int mc_max_clusters()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (g_mc_clusters[dev] == 0) {
+    if (g_mc_clusters[dev].load(std::memory_order_relaxed) == 0) {
         using L = Layout<256, 4, 8, 3, false>;
         auto kern = gemm_blockscaled_kernel<256, 4, 8, 3, false, false, 2>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::dyn_bytes) !=
@@ -1342,12 +1343,13 @@ int mc_max_clusters()
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
-            g_mc_clusters[dev] = -1;
+            g_mc_clusters[dev].store(-1, std::memory_order_relaxed);
         } else {
-            g_mc_clusters[dev] = n;
+            g_mc_clusters[dev].store(n, std::memory_order_relaxed);
         }
     }
-    return g_mc_clusters[dev] > 0 ? g_mc_clusters[dev] : 0;
+    const int n = g_mc_clusters[dev].load(std::memory_order_relaxed);
+    return n > 0 ? n : 0;
 }
 
 bool make_tensor_map_2d(void *map, int dtype_bytes, bool is_float, const void *base, uint64_t inner, uint64_t outer,

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
 }
 
-int g_max_clusters[64];                          // co-resident CTA pairs per device (0: not yet known)
+std::atomic<int> g_max_clusters[64];                          // co-resident CTA pairs per device (0: not yet known)
 
 template <bool OUT_F32>
 cudaError_t launch_pair_variant(const GemmArgs &a, const PairParams &p, int clusters, cudaStream_t stream)
@@ -582,7 +583,7 @@ int pair_max_clusters()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (g_max_clusters[dev] == 0) {
+    if (g_max_clusters[dev].load(std::memory_order_relaxed) == 0) {
         auto kern = gemm_pair_kernel<false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PairLayout::dyn_bytes) !=
             cudaSuccess)
@@ -601,12 +602,13 @@ int pair_max_clusters()
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
-            g_max_clusters[dev] = -1;
+            g_max_clusters[dev].store(-1, std::memory_order_relaxed);
         } else {
-            g_max_clusters[dev] = n;
+            g_max_clusters[dev].store(n, std::memory_order_relaxed);
         }
     }
-    return g_max_clusters[dev] > 0 ? g_max_clusters[dev] : 0;
+    const int n = g_max_clusters[dev].load(std::memory_order_relaxed);
+    return n > 0 ? n : 0;
 }
 
 int pair_tile_n()
