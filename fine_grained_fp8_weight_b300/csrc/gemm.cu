@@ -19,21 +19,25 @@
 //   - warp 1 (one lane) issues 4 tcgen05.mma (K = 32 each) per K group into a
 //     fresh FP32 partial in tensor memory, alternating between two TMEM
 //     buffers so that the next group's MMAs run while this one is promoted;
-//   - warps 4..11 (two promotion warpgroups, one TMEM lane = one output row
-//     per thread, half of the tile's columns each) read each partial with
-//     tcgen05.ld, multiply by sa*sb and add into FP32 registers, then write
-//     the finished tile (BF16 or FP32).
+//   - warps 4..11 (two promotion warpgroups, half of the tile's columns
+//     each) read each partial with tcgen05.ld, multiply by sa*sb and add into
+//     FP32 registers, then write the finished tile (BF16 or FP32).  With
+//     block B scales a thread owns one TMEM lane (one output row); with
+//     per-row B scales it reads the 16x256b shape (4 rows x 32 columns), so
+//     that it needs a quarter of the column scales.
 //   Schedule: tile t runs on CTA t mod grid.  When the tiles leave the last
 //   wave over the SMs partly empty (dense GEMMs, workspace permitting), the
 //   whole waves keep that order and each remaining tile is cut into K pieces
 //   on otherwise idle CTAs; the last piece to finish (an atomic ticket) adds
 //   the FP32 partials in K order and writes the tile.  No CTA waits for
-//   another.
+//   another.  A test switch runs the same kernel in clusters of two CTAs on
+//   vertically adjacent tiles that share the B panel by TMA multicast.
 // gemm_smallm_kernel (decode, dense M <= 128 tokens): the weight tile takes
 // the MMA's M side and the tokens its N side, K is split over the CTAs of a
 // thread-block cluster, which add their partials in split order through
 // distributed shared memory; the same kernel serves the masked grouped layout
-// (per-expert token slots of up to 256 rows with device-side counts) and, for
+// (per-expert token slots of up to 256 rows with device-side counts; the
+// K groups per barrier handshake follow each expert's count) and, for
 // M <= 256, the variant that quantizes BF16 tokens inside the kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
