@@ -32,3 +32,18 @@ def test_oracle_sample_covers_every_gemm_kind():
     for w in works:
         flops, secs, full = bench.oracle_sample(w, 3, 2, seed=0)
         assert flops > 0 and secs > 0 and full >= secs * 0.5, w.name
+
+
+def test_measured_traffic_names_this_build():
+    # the roofline line's DRAM traffic is keyed by the library's version
+    # string; a build that changes a kernel changes the string, and the
+    # prefill GEMMs' ncu totals must be recorded for it (else the bench
+    # line would carry traffic: null)
+    sys.path.insert(0, ROOT)
+    import bench
+    import fine_grained_fp8_weight_b300 as fg
+    version = fg.lib().fgf8_version().decode()
+    entry = bench.MEASURED_TRAFFIC.get(version)
+    assert entry is not None, f"no DRAM traffic recorded for {version}"
+    for op in ("up.gemm", "down.gemm"):
+        assert entry.get(f"prefill_pair_4096x18432x7168/{op}", 0) > 0, op
